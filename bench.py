@@ -1,0 +1,423 @@
+"""Benchmark of the S2 Reducer hot path: encode -> reduce -> decode on one GPU.
+
+One step = s2_encode_batched over the W resident workers' gradients, s2_reduce
+of their bitmaps and sketches, and s2_decode_dense of the aggregate: the whole
+path over one batch of synthetic input, with the inputs already in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0). ``value`` is W*n gradient elements per second
+(Gelem/s) over the K timed steps, whole job. L2 is flushed (a 512 MiB write)
+before every step, outside the timed events. ``roofline`` is the dominant
+kernel (encode) against the measured HBM copy bandwidth; ``path_roofline`` the
+whole step. ``e2e`` times the same path from pinned host memory to host memory
+through the C-ABI call s2_pipeline_dense_host. ``cpu_baseline`` times the CPU
+oracle (test infrastructure, plain C) on the same workload on the host cores.
+
+With ``--impl reference`` the oracle itself is the timed arm (rank 0 only).
+For N > 1 (torchrun), every rank runs an independent replica of the workload
+(weak scaling): the path has no exchange between GPUs.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "S2 encode→reduce→decode Gelem/s and achieved HBM GB/s vs GB300 peak, 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 512 << 20
+
+
+# ---------------------------------------------------------------- byte accounting
+
+def algorithmic_bytes(wl: workloads.Workload, nnz_union: int) -> dict:
+    """Bytes each stage must move at minimum (each structure read/written once).
+
+    encode: read grad, write W bitmaps and W sketches;
+    reduce: read W bitmaps and W sketches, write one bitmap and one sketch;
+    decode: read the bitmap, read at most the sketch (d gathers per set bit,
+            counted up to one full read), write the dense output.
+    """
+    W, n, d, w = wl.W, wl.n, wl.d, wl.w
+    E = wl.elem_bytes
+    BM = 4 * ((n + 31) // 32)
+    SK = 4 * d * w
+    enc = W * n * E + W * BM + W * SK
+    red = W * (SK + BM) + SK + BM
+    dec = BM + min(SK, 4 * d * nnz_union) + 4 * n
+    return {"encode": enc, "reduce": red, "decode": dec, "total": enc + red + dec}
+
+
+def encode_launches(wl: workloads.Workload, l2_bytes: int) -> int:
+    """Kernels one s2_encode_batched call launches: a zero fill and an encode per
+    group of workers whose sketches fit in 40% of L2 together."""
+    sk = 4 * wl.d * wl.w
+    group = max(1, min(wl.W, (l2_bytes * 2 // 5) // sk)) if sk else wl.W
+    return 2 * ((wl.W + group - 1) // group)
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": float(j["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sketch_compressed_sparse_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per encode launch from a committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "encode_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        j = json.load(f)
+    if j.get("source_sha") != kernel_source_sha():
+        return None
+    return j.get("per_workload", {}).get(workload)
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self) -> dict:
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def physical_gpu_index(local: int) -> int:
+    """nvidia-smi index of CUDA device `local` (honours a numeric CUDA_VISIBLE_DEVICES)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local < len(ids) and ids[local].isdigit():
+            return int(ids[local])
+    return local
+
+
+# ---------------------------------------------------------------- distributed helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def combine_over_ranks(elapsed_s: float, units: float, world: int, device=None):
+    """(max elapsed over ranks, sum of units over ranks). Single process: identity."""
+    if world <= 1:
+        return elapsed_s, units
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def time_oracle(wl: workloads.Workload, G: np.ndarray, reps: int) -> dict:
+    import oracle
+
+    oracle.build()
+    ts = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        oracle.pipeline(G, wl.d, wl.w, wl.seed, dtype=wl.dtype)
+        ts.append(time.perf_counter() - t0)
+    t = statistics.median(ts)
+    return {"seconds": t, "reps": reps, "value": wl.W * wl.n / t / 1e9}
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, wl, world, rank, local):
+    import torch
+
+    import sketch_compressed_sparse_gb300 as s2
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 << 20))
+    W, n, d, w, seed = wl.W, wl.n, wl.d, wl.w, wl.seed
+    nnz_u = wl.union_nnz()
+    grad = wl.dense_torch(dev)
+    bitmaps, sketches = s2.alloc_encode_outputs(W, n, d, w, dev)
+    bitmap = torch.empty(s2.nwords(n), dtype=torch.int32, device=dev)
+    sketch = torch.empty((d, w), dtype=torch.float32, device=dev)
+    out = torch.empty(n, dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        s2.s2_encode_batched(grad, d, w, seed, bitmaps, sketches)
+        s2.s2_reduce(bitmaps, sketches, n, d, w, bitmap, sketch)
+        s2.s2_decode_dense(bitmap, sketch, n, d, w, seed, out)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(physical_gpu_index(local)) as clk:
+        wall0 = time.perf_counter()
+        for k in range(K):
+            flush.fill_(float(k & 7))
+            e = ev[k]
+            e[0].record(stream)
+            s2.s2_encode_batched(grad, d, w, seed, bitmaps, sketches)
+            e[1].record(stream)
+            s2.s2_reduce(bitmaps, sketches, n, d, w, bitmap, sketch)
+            e[2].record(stream)
+            s2.s2_decode_dense(bitmap, sketch, n, d, w, seed, out)
+            e[3].record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - wall0
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+    enc_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
+    red_ms = sum(e[1].elapsed_time(e[2]) for e in ev)
+    dec_ms = sum(e[2].elapsed_time(e[3]) for e in ev)
+    total_ms = enc_ms + red_ms + dec_ms
+    elapsed, units = combine_over_ranks(total_ms / 1e3, float(W * n * K), world, dev)
+    value = units / elapsed / 1e9
+
+    by = algorithmic_bytes(wl, nnz_u)
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"]
+    enc_s = enc_ms / 1e3 / K
+    n_enc = encode_launches(wl, l2)
+    ach_enc = by["encode"] / enc_s / 1e9
+    path_gbs = by["total"] / (total_ms / 1e3 / K) / 1e9
+    traffic = recorded_traffic(args.config)
+
+    res = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "Gelem/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / K, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32" if wl.dtype == "f32" else "bf16",
+        "data": "synthetic",
+        "config": dict(wl.describe(), nnz_union=nnz_u, l2="flushed before every step (512 MiB write)",
+                       parallelism=f"replicas{world}" if world > 1 else "single GPU, W workers resident"),
+        "stages_ms_per_step": {"encode": round(enc_ms / K, 5), "reduce": round(red_ms / K, 5),
+                               "decode": round(dec_ms / K, 5)},
+        "roofline": {"kernel": "encode (zero fill + fused bitmap/sketch scatter)", "bound": "hbm",
+                     "achieved": round(ach_enc, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(ach_enc / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_step": by["encode"], "launches_per_step": n_enc,
+                     "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"},
+        "path_roofline": {"bound": "hbm", "achieved": round(path_gbs, 1), "peak": peak, "unit": "GB/s",
+                          "frac": round(path_gbs / peak, 4), "algorithmic_bytes_per_step": by["total"],
+                          "stage_frac": {k: round(by[k] / (v / 1e3 / K) / 1e9 / peak, 4) for k, v in
+                                         (("encode", enc_ms), ("reduce", red_ms), ("decode", dec_ms))}},
+        "gpu_launches": K * (n_enc + 2),
+        "wall_ms_timed_region": round(wall * 1e3, 3),
+    }
+    res["clocks"] = clk.summary()
+
+    if not args.no_e2e:
+        res["e2e"] = run_e2e(args, wl, dev, s2)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        G = wl.dense()
+        o = time_oracle(wl, G, reps=1)
+        res["cpu_baseline"] = {"value": round(o["value"], 5), "unit": "Gelem/s", "cores": 1, "kind": "oracle",
+                               "sample": f"one full encode->reduce->decode of this workload on the host "
+                                         f"({o['seconds']:.2f} s, single thread, plain C, fp64)"}
+    return res
+
+
+def run_e2e(args, wl, dev, s2):
+    """Host pinned grad -> device -> path -> host out, through s2_pipeline_dense_host."""
+    import torch
+
+    G = wl.dense()
+    hg = torch.from_numpy(G if wl.dtype == "f32" else G.view(np.int16)).pin_memory()
+    if wl.dtype == "bf16":
+        hg = hg.view(torch.bfloat16)
+    ho = torch.empty(wl.n, dtype=torch.float32).pin_memory()
+    ws = torch.empty(s2.s2_pipeline_workspace_size(hg.dtype, wl.W, wl.n, wl.d, wl.w), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        s2.s2_pipeline_dense_host(hg, wl.d, wl.w, wl.seed, ho, ws)
+    torch.cuda.synchronize(dev)
+    K = max(3, min(args.steps, args.e2e_steps))
+    t = 0.0
+    for _ in range(K):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        s2.s2_pipeline_dense_host(hg, wl.d, wl.w, wl.seed, ho, ws)
+        b.record(stream)
+        b.synchronize()
+        t += a.elapsed_time(b) / 1e3
+    return {"value": round(wl.W * wl.n * K / t / 1e9, 3), "unit": "Gelem/s",
+            "h2d_bytes_per_step": int(wl.W * wl.n * wl.elem_bytes), "d2h_bytes_per_step": int(4 * wl.n),
+            "steps": K, "ms_per_step": round(t / K * 1e3, 4)}
+
+
+# ---------------------------------------------------------------- reference arm (the oracle)
+
+def run_reference(args, wl):
+    G = wl.dense()
+    one = time_oracle(wl, G, reps=1)  # also the untimed warm-up
+    budget_s = 150.0
+    K = max(1, min(args.steps, int(budget_s // max(one["seconds"], 1e-3))))
+    o = time_oracle(wl, G, reps=K)
+    v = round(o["value"], 5)
+    sample = (f"{K} full encode->reduce->decode passes of this workload (of {args.steps} requested; bounded to "
+              f"~{budget_s:.0f} s), single thread, plain C, fp64")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": v,
+        "unit": "Gelem/s",
+        "n_gpus": 1,
+        "steps": K,
+        "warmup": 1,
+        "ms_per_step": round(o["seconds"] * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": dict(wl.describe(), nnz_union=wl.union_nnz()),
+        "cpu_baseline": {"value": v, "unit": "Gelem/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "Gelem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="embedding", choices=["tiny", "embedding", "topk", "large_lm"])
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle timing")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--out", default=None, help="also append the JSON line to this file")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours" and args.steps > 5:
+        ap.error("use at least 3 warm-up steps")
+
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        res = run_reference(args, workloads.by_name(args.config))
+    else:
+        if world > 1:
+            import torch
+            import torch.distributed as dist
+
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        res = run_ours(args, workloads.by_name(args.config), world, rank, local)
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+        if rank != 0:
+            return 0
+    line = json.dumps(res)
+    print(line, flush=True)
+    if args.out:
+        with open(args.out, "a") as f:
+            f.write(line + "\n")
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

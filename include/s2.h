@@ -1,0 +1,187 @@
+/*
+ * s2.h -- C ABI of libs2, the GB300 (sm_103a) S2 Reducer hot path.
+ *
+ * The operations follow "S2 Reducer: High-Performance Sparse Communication
+ * to Accelerate Distributed Deep Learning" (Ge et al.), Section 3.1 and
+ * Algorithm 1 (Sparse-Sketch Reducer):
+ *   encode  -- each worker marks its nonzero positions in a bitmap and adds
+ *              every nonzero into a d x w count-sketch (the compression phase);
+ *   reduce  -- the workers' sketches are summed and their bitmaps OR-ed (the
+ *              AllReduce(S, C) step; here all workers live on one GPU);
+ *   decode  -- every position set in the aggregated bitmap is queried as the
+ *              median over the rows of its signed buckets (the decompression
+ *              phase), giving a dense vector or an (index, value) list.
+ *
+ * Notation: n = gradient length, d = sketch rows, w = buckets per row,
+ * W = workers. (The paper writes d for the length, r for the rows and c or m
+ * for the buckets.)
+ *
+ * Common conventions
+ *  - Every pointer argument is DEVICE memory owned by the caller, except the
+ *    host_* arguments of s2_pipeline_dense_host. The library allocates
+ *    nothing and keeps no pointer after a call returns.
+ *  - Every call is asynchronous on `stream` (NULL = the legacy default
+ *    stream) and never synchronises the host. Validation errors are returned
+ *    before anything is launched; a failed launch returns S2_ERR_CUDA.
+ *  - Outputs are overwritten, never accumulated into. Outputs must not
+ *    overlap inputs (S2_ERR_INVALID_ARG).
+ *  - Gradient, bitmap, sketch and dense-output base pointers must be 16-byte
+ *    aligned (S2_ERR_ALIGNMENT). Other arrays need their natural alignment.
+ *  - Positions are 32-bit: n must be below 2^32 (S2_ERR_UNSUPPORTED).
+ *  - Bitmap layout: position i is bit (i % 32) of 32-bit word i / 32, least
+ *    significant bit first; nw = ceil(n / 32) words; bits at positions >= n
+ *    are written as 0.
+ *  - Sketch layout: float32, row-major [d][w]; batched arrays are
+ *    worker-major: grad[W][n], bitmaps[W][nw], sketches[W][d][w].
+ *  - A position is nonzero iff its bit pattern without the sign bit is not
+ *    zero: -0.0 counts as zero, subnormals count as nonzero. NaN and Inf
+ *    inputs are outside the contract.
+ *  - Hash family (the paper leaves it open): with fmix32 the 32-bit
+ *    MurmurHash3 finalizer and G = 0x9E3779B9, row j has keys
+ *    kh_j = fmix32(seed ^ G*(2j+1)) and ks_j = fmix32(seed ^ G*(2j+2))
+ *    (mod 2^32); bucket h_j(i) = (fmix32(i ^ kh_j) * w) >> 32 computed in
+ *    64 bits; sign s_j(i) = -1 if fmix32(i ^ ks_j) >= 2^31, else +1.
+ *  - The library is stateless and thread-safe; no exception crosses the ABI.
+ */
+#ifndef S2_H
+#define S2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define S2_API __attribute__((visibility("default")))
+#else
+#define S2_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream; NULL selects the legacy default stream. */
+typedef struct CUstream_st *s2_stream_t;
+
+typedef enum {
+    S2_OK = 0,
+    S2_ERR_INVALID_ARG = 1, /* null pointer, bad d/w/W, overlapping buffers, small workspace */
+    S2_ERR_ALIGNMENT = 2,   /* a pointer misses its required alignment */
+    S2_ERR_UNSUPPORTED = 3, /* n >= 2^32 or another size the library does not handle */
+    S2_ERR_CUDA = 4         /* a CUDA runtime call or kernel launch failed */
+} s2_status;
+
+typedef enum {
+    S2_F32 = 0, /* IEEE float32 gradient */
+    S2_BF16 = 1 /* bfloat16 gradient (the sketch and the decoded values stay float32) */
+} s2_dtype;
+
+#define S2_MAX_ROWS 16u
+
+/* Sketch shape and hash seed. d in [1, S2_MAX_ROWS]; w in [1, 2^31]. */
+typedef struct {
+    uint32_t d;
+    uint32_t w;
+    uint32_t seed;
+} s2_params;
+
+/*
+ * s2_encode -- compression phase for ONE worker (Section 3.1 "Compressing
+ * Sparse Gradient"; Algorithm 1, compression loop).
+ *   grad   [n] elements of type dt (16-byte aligned).
+ *   bitmap [nw] uint32 out: bit i set iff grad[i] is nonzero.
+ *   sketch [d][w] float32 out: zeroed, then sketch[j][h_j(i)] += s_j(i)*grad[i]
+ *          for every nonzero i and row j. float32 adds in an unspecified order.
+ * n = 0 is valid (the sketch is zeroed, no bitmap word is written).
+ */
+S2_API s2_status s2_encode(const void *grad, s2_dtype dt, uint64_t n, s2_params p, uint32_t *bitmap,
+                    float *sketch, s2_stream_t stream);
+
+/*
+ * s2_encode_batched -- s2_encode on W workers at once.
+ *   grad     [W][n] (worker k starts at element k*n), 16-byte aligned base.
+ *   bitmaps  [W][nw] uint32 out.   sketches [W][d][w] float32 out.
+ * W = 0 is valid and does nothing. When n*sizeof(dt) is not a multiple of 16
+ * the workers' rows are not 16-byte aligned and a scalar-load kernel is used.
+ */
+S2_API s2_status s2_encode_batched(const void *grad, s2_dtype dt, uint32_t W, uint64_t n, s2_params p,
+                            uint32_t *bitmaps, float *sketches, s2_stream_t stream);
+
+/*
+ * s2_reduce -- the AllReduce(S, C) of Algorithm 1 (Section 3.1 "Collecting
+ * Sparse-Sketch with AllReduce"), with all W workers resident on this GPU.
+ *   bitmaps [W][nw], sketches [W][d][w]  in.
+ *   bitmap_out [nw] = OR over k of bitmaps[k];
+ *   sketch_out [d][w] = sum over k of sketches[k], added in the fixed order
+ *   k = 0, 1, ..., W-1 (deterministic). W = 0 writes zeros.
+ */
+S2_API s2_status s2_reduce(const uint32_t *bitmaps, const float *sketches, uint32_t W, uint64_t n,
+                    s2_params p, uint32_t *bitmap_out, float *sketch_out, s2_stream_t stream);
+
+/*
+ * s2_decode_dense -- decompression phase with a dense output (Section 3.1
+ * "Decompressing Sparse Gradient"; Algorithm 1, decompression loop).
+ *   bitmap [nw], sketch [d][w] in; out [n] float32 (16-byte aligned).
+ *   For every set bit i: out[i] = scale * median_j( s_j(i) * sketch[j][h_j(i)] );
+ *   the median of an even number of rows is the mean of the two middle values.
+ *   Every unset position receives exactly +0.0f.
+ */
+S2_API s2_status s2_decode_dense(const uint32_t *bitmap, const float *sketch, uint64_t n, s2_params p,
+                          float scale, float *out, s2_stream_t stream);
+
+/* Device workspace bytes that s2_decode_compact needs for length n. */
+S2_API s2_status s2_decode_workspace_size(uint64_t n, size_t *bytes);
+
+/*
+ * s2_decode_compact -- decompression phase with a compacted output: the set
+ * positions of the bitmap in ascending order and their estimates.
+ *   idx_out [capacity] uint32, val_out [capacity] float32: entry t holds the
+ *   t-th set position and its estimate (same value as s2_decode_dense).
+ *   count_out: ONE uint64 in device memory, receives the number of set bits
+ *   (always the true count, even when it exceeds capacity; entries at
+ *   t >= capacity are not written).
+ *   workspace: device scratch of at least s2_decode_workspace_size(n) bytes,
+ *   16-byte aligned; its contents on entry do not matter.
+ * Compaction is exact and deterministic: no inter-block waiting is involved.
+ */
+S2_API s2_status s2_decode_compact(const uint32_t *bitmap, const float *sketch, uint64_t n, s2_params p,
+                            float scale, uint32_t *idx_out, float *val_out, uint64_t capacity,
+                            uint64_t *count_out, void *workspace, size_t workspace_bytes,
+                            s2_stream_t stream);
+
+/*
+ * s2_hash -- the bucket and sign hashes of m given positions, for checking.
+ *   idx [m] uint32 in; bucket_out [d][m] uint32 and sign_out [d][m] int8
+ *   (+1 or -1) out, row-major by row j.
+ */
+S2_API s2_status s2_hash(const uint32_t *idx, uint64_t m, s2_params p, uint32_t *bucket_out,
+                  int8_t *sign_out, s2_stream_t stream);
+
+/* Device workspace bytes that s2_pipeline_dense_host needs. */
+S2_API s2_status s2_pipeline_workspace_size(s2_dtype dt, uint32_t W, uint64_t n, s2_params p,
+                                     size_t *bytes);
+
+/*
+ * s2_pipeline_dense_host -- the whole path from HOST memory to HOST memory:
+ * copy grad [W][n] to the device, s2_encode_batched, s2_reduce,
+ * s2_decode_dense, and copy the decoded [n] float32 vector back.
+ *   host_grad / host_out: host memory; pinned (page-locked) memory makes the
+ *   copies asynchronous, pageable memory makes them synchronous.
+ *   workspace: device scratch of s2_pipeline_workspace_size bytes, 16-byte
+ *   aligned. The call returns once the work is queued on `stream`; host_out
+ *   is valid after the stream is synchronised.
+ */
+S2_API s2_status s2_pipeline_dense_host(const void *host_grad, s2_dtype dt, uint32_t W, uint64_t n,
+                                 s2_params p, float scale, float *host_out, void *workspace,
+                                 size_t workspace_bytes, s2_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+S2_API const char *s2_status_string(s2_status st);
+
+/* Library version string (static). */
+S2_API const char *s2_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* S2_H */

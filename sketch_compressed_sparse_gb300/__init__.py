@@ -1,0 +1,226 @@
+"""Python binding of libs2, the sm_103a S2 Reducer hot path.
+
+Argument marshalling only: every function below checks the torch tensors it
+is given (device, dtype, contiguity, sizes), passes their device pointers and
+the current CUDA stream to the C ABI declared in ``include/s2.h``, and raises
+``S2Error`` on a non-OK status. All computation happens in the CUDA kernels
+of ``libs2.so``; there is no fallback. If the library has not been built,
+importing this package raises ``ImportError`` (build it with
+``python -m sketch_compressed_sparse_gb300.build``).
+
+PyTorch is used for device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+__all__ = [
+    "S2Error",
+    "lib_path",
+    "nwords",
+    "s2_encode",
+    "s2_encode_batched",
+    "s2_reduce",
+    "s2_decode_dense",
+    "s2_decode_workspace_size",
+    "s2_decode_compact",
+    "s2_hash",
+    "s2_pipeline_workspace_size",
+    "s2_pipeline_dense_host",
+    "s2_status_string",
+    "s2_version",
+    "S2_F32",
+    "S2_BF16",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_lib", "libs2.so")
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(
+        f"libs2.so not found at {_LIB_PATH}: build the CUDA library first "
+        "(python -m sketch_compressed_sparse_gb300.build)"
+    )
+
+_lib = ctypes.CDLL(_LIB_PATH)
+
+S2_OK, S2_ERR_INVALID_ARG, S2_ERR_ALIGNMENT, S2_ERR_UNSUPPORTED, S2_ERR_CUDA = range(5)
+S2_F32, S2_BF16 = 0, 1
+
+
+class Params(ctypes.Structure):
+    _fields_ = [("d", ctypes.c_uint32), ("w", ctypes.c_uint32), ("seed", ctypes.c_uint32)]
+
+
+_u32, _u64, _i32, _f32, _vp, _sz = (ctypes.c_uint32, ctypes.c_uint64, ctypes.c_int, ctypes.c_float,
+                                     ctypes.c_void_p, ctypes.c_size_t)
+
+
+def _sig(name, args, res=_i32):
+    f = getattr(_lib, name)
+    f.argtypes = args
+    f.restype = res
+    return f
+
+
+_enc = _sig("s2_encode", [_vp, _i32, _u64, Params, _vp, _vp, _vp])
+_encb = _sig("s2_encode_batched", [_vp, _i32, _u32, _u64, Params, _vp, _vp, _vp])
+_red = _sig("s2_reduce", [_vp, _vp, _u32, _u64, Params, _vp, _vp, _vp])
+_decd = _sig("s2_decode_dense", [_vp, _vp, _u64, Params, _f32, _vp, _vp])
+_decws = _sig("s2_decode_workspace_size", [_u64, ctypes.POINTER(_sz)])
+_decc = _sig("s2_decode_compact", [_vp, _vp, _u64, Params, _f32, _vp, _vp, _u64, _vp, _vp, _sz, _vp])
+_hash = _sig("s2_hash", [_vp, _u64, Params, _vp, _vp, _vp])
+_pws = _sig("s2_pipeline_workspace_size", [_i32, _u32, _u64, Params, ctypes.POINTER(_sz)])
+_pipe = _sig("s2_pipeline_dense_host", [_vp, _i32, _u32, _u64, Params, _f32, _vp, _vp, _sz, _vp])
+_stat = _sig("s2_status_string", [_i32], ctypes.c_char_p)
+_ver = _sig("s2_version", [], ctypes.c_char_p)
+
+
+class S2Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {_stat(status).decode()} ({status})")
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def s2_status_string(status: int) -> str:
+    return _stat(status).decode()
+
+
+def s2_version() -> str:
+    return _ver().decode()
+
+
+def nwords(n: int) -> int:
+    return (n + 31) // 32
+
+
+def _check(status: int, where: str):
+    if status != S2_OK:
+        raise S2Error(status, where)
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dev(t: Optional[torch.Tensor], name: str, dtypes, numel: Optional[int] = None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} holds {t.numel()} elements, needs {numel}")
+    return t.data_ptr() if t.numel() else None
+
+
+_U32 = (torch.int32, torch.uint32) if hasattr(torch, "uint32") else (torch.int32,)
+_GRAD = (torch.float32, torch.bfloat16)
+
+
+def _dtype_code(g: torch.Tensor) -> int:
+    return S2_F32 if g.dtype == torch.float32 else S2_BF16
+
+
+def s2_encode(grad: torch.Tensor, d: int, w: int, seed: int, bitmap: torch.Tensor, sketch: torch.Tensor,
+              stream=None) -> None:
+    """One worker: grad [n] -> bitmap [nw] (int32 words), sketch [d, w] float32."""
+    n = grad.numel()
+    _check(_enc(_dev(grad, "grad", _GRAD), _dtype_code(grad), n, Params(d, w, seed),
+                _dev(bitmap, "bitmap", _U32, nwords(n)), _dev(sketch, "sketch", (torch.float32,), d * w),
+                _stream(stream)), "s2_encode")
+
+
+def s2_encode_batched(grad: torch.Tensor, d: int, w: int, seed: int, bitmaps: torch.Tensor,
+                      sketches: torch.Tensor, stream=None) -> None:
+    """W workers: grad [W, n] -> bitmaps [W, nw], sketches [W, d, w]."""
+    if grad.dim() != 2:
+        raise ValueError("grad must be [W, n]")
+    W, n = grad.shape
+    _check(_encb(_dev(grad, "grad", _GRAD), _dtype_code(grad), W, n, Params(d, w, seed),
+                 _dev(bitmaps, "bitmaps", _U32, W * nwords(n)),
+                 _dev(sketches, "sketches", (torch.float32,), W * d * w), _stream(stream)), "s2_encode_batched")
+
+
+def s2_reduce(bitmaps: torch.Tensor, sketches: torch.Tensor, n: int, d: int, w: int, bitmap_out: torch.Tensor,
+              sketch_out: torch.Tensor, stream=None) -> None:
+    """bitmaps [W, nw], sketches [W, d, w] -> bitmap_out [nw] (OR), sketch_out [d, w] (sum)."""
+    W = sketches.shape[0] if sketches.dim() == 3 else sketches.numel() // max(d * w, 1)
+    _check(_red(_dev(bitmaps, "bitmaps", _U32, W * nwords(n)),
+                _dev(sketches, "sketches", (torch.float32,), W * d * w), W, n, Params(d, w, 0),
+                _dev(bitmap_out, "bitmap_out", _U32, nwords(n)),
+                _dev(sketch_out, "sketch_out", (torch.float32,), d * w), _stream(stream)), "s2_reduce")
+
+
+def s2_decode_dense(bitmap: torch.Tensor, sketch: torch.Tensor, n: int, d: int, w: int, seed: int,
+                    out: torch.Tensor, scale: float = 1.0, stream=None) -> None:
+    """bitmap [nw], sketch [d, w] -> out [n] float32 (median estimates, +0.0 at unset bits)."""
+    _check(_decd(_dev(bitmap, "bitmap", _U32, nwords(n)), _dev(sketch, "sketch", (torch.float32,), d * w), n,
+                 Params(d, w, seed), scale, _dev(out, "out", (torch.float32,), n), _stream(stream)),
+           "s2_decode_dense")
+
+
+def s2_decode_workspace_size(n: int) -> int:
+    b = _sz()
+    _check(_decws(n, ctypes.byref(b)), "s2_decode_workspace_size")
+    return int(b.value)
+
+
+def s2_decode_compact(bitmap: torch.Tensor, sketch: torch.Tensor, n: int, d: int, w: int, seed: int,
+                      idx_out: torch.Tensor, val_out: torch.Tensor, count_out: torch.Tensor,
+                      workspace: torch.Tensor, scale: float = 1.0, stream=None) -> None:
+    """bitmap, sketch -> idx_out [cap] int32, val_out [cap] float32, count_out [1] int64 (device)."""
+    cap = min(idx_out.numel(), val_out.numel())
+    _check(_decc(_dev(bitmap, "bitmap", _U32, nwords(n)), _dev(sketch, "sketch", (torch.float32,), d * w), n,
+                 Params(d, w, seed), scale, _dev(idx_out, "idx_out", _U32), _dev(val_out, "val_out", (torch.float32,)),
+                 cap, _dev(count_out, "count_out", (torch.int64,), 1), _dev(workspace, "workspace", (torch.uint8,)),
+                 workspace.numel(), _stream(stream)), "s2_decode_compact")
+
+
+def s2_hash(idx: torch.Tensor, d: int, w: int, seed: int, bucket_out: torch.Tensor, sign_out: torch.Tensor,
+            stream=None) -> None:
+    """idx [m] -> bucket_out [d, m] int32, sign_out [d, m] int8."""
+    m = idx.numel()
+    _check(_hash(_dev(idx, "idx", _U32), m, Params(d, w, seed), _dev(bucket_out, "bucket_out", _U32, d * m),
+                 _dev(sign_out, "sign_out", (torch.int8,), d * m), _stream(stream)), "s2_hash")
+
+
+def s2_pipeline_workspace_size(dtype: torch.dtype, W: int, n: int, d: int, w: int) -> int:
+    b = _sz()
+    _check(_pws(S2_F32 if dtype == torch.float32 else S2_BF16, W, n, Params(d, w, 0), ctypes.byref(b)),
+           "s2_pipeline_workspace_size")
+    return int(b.value)
+
+
+def s2_pipeline_dense_host(host_grad: torch.Tensor, d: int, w: int, seed: int, host_out: torch.Tensor,
+                           workspace: torch.Tensor, scale: float = 1.0, stream=None) -> None:
+    """HOST grad [W, n] (pinned for async copies) -> HOST out [n]; queued on the stream."""
+    if host_grad.is_cuda or host_out.is_cuda:
+        raise ValueError("s2_pipeline_dense_host takes host tensors")
+    if host_grad.dim() != 2 or host_grad.dtype not in _GRAD or not host_grad.is_contiguous():
+        raise ValueError("host_grad must be a contiguous [W, n] float32/bfloat16 tensor")
+    W, n = host_grad.shape
+    if host_out.dtype != torch.float32 or host_out.numel() < n or not host_out.is_contiguous():
+        raise ValueError("host_out must be a contiguous float32 tensor of n elements")
+    _check(_pipe(host_grad.data_ptr(), _dtype_code(host_grad), W, n, Params(d, w, seed), scale,
+                 host_out.data_ptr(), _dev(workspace, "workspace", (torch.uint8,)), workspace.numel(),
+                 _stream(stream)), "s2_pipeline_dense_host")
+
+
+# ---- allocation helpers (torch owns the memory; the library never allocates) ----
+
+def alloc_encode_outputs(W: int, n: int, d: int, w: int, device="cuda") -> Tuple[torch.Tensor, torch.Tensor]:
+    return (torch.empty((W, nwords(n)), dtype=torch.int32, device=device),
+            torch.empty((W, d, w), dtype=torch.float32, device=device))

@@ -1,0 +1,340 @@
+// Decompression phase of S2 Reducer ("S2 Reducer", Section 3.1
+// "Decompressing Sparse Gradient"; Algorithm 1, decompression loop): recover
+// the set positions from the aggregated bitmap and, for each, take the median
+// over the d rows of s_j(i) * S[j][h_j(i)].
+//
+// Design: a warp owns 512 consecutive positions (16 bitmap words). Lanes
+// 0..15 load the words; every lane then owns 16 positions (4 chunks of 4
+// consecutive positions, so the dense output leaves as 16-byte streaming
+// stores). A lane walks only its set positions, two per step so that 2*d
+// independent gathers from the L2-resident sketch are in flight, and keeps
+// the results in registers. Unset positions are written as +0.0f with the
+// same stores.
+//
+// The compacted output uses three kernels and no inter-block waiting:
+// per-tile popcounts, one block that scans the tile totals (and writes the
+// final count), and a writer that recomputes the in-tile offsets with warp
+// scans and writes (index, value) pairs in ascending order.
+#include "s2_internal.h"
+
+namespace s2 {
+namespace {
+
+__device__ __forceinline__ void load_keys(const RowKeys& k, uint32_t* s_kh, uint32_t* s_ks) {
+    if (threadIdx.x < kMaxRows) {
+        s_kh[threadIdx.x] = k.kh[threadIdx.x];
+        s_ks[threadIdx.x] = k.ks[threadIdx.x];
+    }
+    __syncthreads();
+}
+
+// Load the d signed estimates of position i.
+template <int D>
+__device__ __forceinline__ void gather(float (&e)[(D > 0 ? D : kMaxRows)], const float* __restrict__ sk,
+                                       uint32_t i, int d, uint32_t w, const uint32_t* s_kh,
+                                       const uint32_t* s_ks) {
+#pragma unroll
+    for (int j = 0; j < (D > 0 ? D : kMaxRows); ++j) {
+        if (D > 0 || j < d) {
+            const uint32_t b = bucket_of(i, s_kh[j], w);
+            const uint32_t sb = signbit_of(i, s_ks[j]);
+            e[j] = apply_sign(__ldg(sk + (uint64_t)j * w + b), sb);
+        } else {
+            e[j] = 0.f;
+        }
+    }
+}
+
+// Bitmap word wi, with the bits at positions >= n cleared (0 past the end).
+__device__ __forceinline__ uint32_t load_word(const uint32_t* __restrict__ bm, uint64_t wi, uint64_t nw, uint64_t n) {
+    if (wi >= nw) return 0u;
+    uint32_t v = __ldg(bm + wi);
+    if (wi == nw - 1 && (n & 31)) v &= (1u << (n & 31)) - 1u;
+    return v;
+}
+
+// Position of slot `slot` of this lane inside a 512-position task.
+__device__ __forceinline__ uint32_t slot_pos(int slot, int lane) {
+    return (uint32_t)((slot >> 2) * 128 + lane * 4 + (slot & 3));
+}
+
+// This lane's 16 slots of a task as a bit mask (slot 4u + c is bit c of the
+// nibble of word 4u + lane/8 at nibble position lane%8). `my_word` is the
+// word held by lane L = word L of the task (lanes 0..15).
+__device__ __forceinline__ uint32_t lane_mask(uint32_t my_word, int lane) {
+    uint32_t mask = 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const uint32_t wv = __shfl_sync(kFull, my_word, u * 4 + (lane >> 3));
+        mask |= ((wv >> (4 * (lane & 7))) & 0xfu) << (4 * u);
+    }
+    return mask;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) decode_dense_kernel(DecodeArgs a, float* __restrict__ out) {
+    __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
+    load_keys(a.keys, s_kh, s_ks);
+    const int lane = threadIdx.x & 31;
+    const uint64_t ntasks = (a.n + kTaskElems - 1) / kTaskElems;
+    const uint64_t nwarps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
+    for (uint64_t t = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < ntasks; t += nwarps) {
+        const uint64_t e0 = t * kTaskElems;
+        const uint64_t wi = t * kTaskWords + lane;
+        const uint32_t my_word = lane < kTaskWords ? load_word(a.bitmap, wi, a.nw, a.n) : 0u;
+        uint32_t mask = lane_mask(my_word, lane);
+        float r[16];
+#pragma unroll
+        for (int s = 0; s < 16; ++s) r[s] = 0.f;
+        while (mask) {
+            const int s0 = __ffs(mask) - 1;
+            mask &= mask - 1;
+            const bool two = mask != 0;
+            const int s1 = two ? __ffs(mask) - 1 : s0;
+            if (two) mask &= mask - 1;
+            float e0v[(D > 0 ? D : kMaxRows)], e1v[(D > 0 ? D : kMaxRows)];
+            gather<D>(e0v, a.sketch, (uint32_t)e0 + slot_pos(s0, lane), a.d, a.w, s_kh, s_ks);
+            gather<D>(e1v, a.sketch, (uint32_t)e0 + slot_pos(s1, lane), a.d, a.w, s_kh, s_ks);
+            const float v0 = a.scale * median_rows<D>(e0v, a.d);
+            const float v1 = a.scale * median_rows<D>(e1v, a.d);
+#pragma unroll
+            for (int s = 0; s < 16; ++s) {
+                r[s] = (s == s0) ? v0 : r[s];
+                r[s] = (two && s == s1) ? v1 : r[s];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint64_t e = e0 + u * 128 + lane * 4;
+            if (e + 4 <= a.n) {
+                st_stream_f4(out + e, make_float4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]));
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if (e + c < a.n) out[e + c] = r[4 * u + c];
+            }
+        }
+    }
+}
+
+// ---- compacted output -------------------------------------------------------
+
+__device__ __forceinline__ uint32_t block_sum(uint32_t v, uint32_t* s_tmp) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    if (lane == 0) s_tmp[warp] = v;
+    __syncthreads();
+    uint32_t tot = 0;
+    if (threadIdx.x < 32) {
+        tot = (lane < (int)(blockDim.x >> 5)) ? s_tmp[lane] : 0u;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(kFull, tot, o);
+    }
+    __syncthreads();
+    return tot;  // valid in thread 0
+}
+
+// Set bits per tile of kCompactTileWords words (one word per thread).
+__global__ void __launch_bounds__(kThreads)
+    compact_count_kernel(const uint32_t* __restrict__ bitmap, uint64_t nw, uint64_t n, uint64_t tiles,
+                         uint32_t* __restrict__ counts) {
+    __shared__ uint32_t s_tmp[kThreads / 32];
+    for (uint64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+        const uint64_t wi = t * kCompactTileWords + threadIdx.x;
+        const uint32_t c = __popc(load_word(bitmap, wi, nw, n));
+        const uint32_t tot = block_sum(c, s_tmp);
+        if (threadIdx.x == 0) counts[t] = tot;
+    }
+}
+
+// Exclusive scan of the tile counts by one block; writes the total count.
+constexpr int kScanThreads = 1024;
+__global__ void __launch_bounds__(kScanThreads)
+    compact_scan_kernel(const uint32_t* __restrict__ counts, uint64_t tiles, uint32_t* __restrict__ offsets,
+                        unsigned long long* __restrict__ count_out) {
+    __shared__ unsigned long long s_warp[kScanThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint64_t per = (tiles + kScanThreads - 1) / kScanThreads;
+    const uint64_t lo = threadIdx.x * per;
+    const uint64_t hi = lo + per < tiles ? lo + per : tiles;
+    unsigned long long local = 0;
+    for (uint64_t x = lo; x < hi; ++x) local += counts[x];
+    // inclusive warp scan of the per-thread sums
+    unsigned long long incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        unsigned long long y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        unsigned long long v = s_warp[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            unsigned long long y = __shfl_up_sync(kFull, v, o);
+            if (lane >= o) v += y;
+        }
+        s_warp[lane] = v;  // inclusive over warps
+    }
+    __syncthreads();
+    unsigned long long run = (warp > 0 ? s_warp[warp - 1] : 0ull) + incl - local;
+    for (uint64_t x = lo; x < hi; ++x) {
+        offsets[x] = (uint32_t)run;
+        run += counts[x];
+    }
+    if (threadIdx.x == kScanThreads - 1) *count_out = s_warp[31];
+}
+
+// Writer: block = tile of 256 words = 16 tasks of 512 positions; warp w
+// handles tasks 2w and 2w+1 of the tile.
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+    compact_write_kernel(DecodeArgs a, uint64_t tiles, const uint32_t* __restrict__ offsets, uint32_t* __restrict__ idx_out,
+                         float* __restrict__ val_out, uint64_t capacity) {
+    __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
+    __shared__ uint32_t s_task[16];
+    load_keys(a.keys, s_kh, s_ks);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (uint64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        uint32_t words[2], excl[2], tot[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint64_t task = tile * 16 + warp * 2 + h;
+            const uint64_t wi = task * kTaskWords + lane;
+            words[h] = lane < kTaskWords ? load_word(a.bitmap, wi, a.nw, a.n) : 0u;
+            const uint32_t c = __popc(words[h]);
+            uint32_t incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                uint32_t y = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o) incl += y;
+            }
+            excl[h] = incl - c;
+            tot[h] = __shfl_sync(kFull, incl, 31);
+        }
+        if (lane == 0) {
+            s_task[warp * 2] = tot[0];
+            s_task[warp * 2 + 1] = tot[1];
+        }
+        __syncthreads();
+        uint32_t base = offsets[tile];
+        for (int q = 0; q < warp * 2; ++q) base += s_task[q];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint64_t task = tile * 16 + warp * 2 + h;
+            const uint64_t e0 = task * kTaskElems;
+            const uint32_t tbase = base + (h ? tot[0] : 0u);
+            uint32_t mask = lane_mask(words[h], lane);
+            uint32_t wv[4], wo[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                wv[u] = __shfl_sync(kFull, words[h], u * 4 + (lane >> 3));
+                wo[u] = __shfl_sync(kFull, excl[h], u * 4 + (lane >> 3));
+            }
+            while (mask) {
+                const int s0 = __ffs(mask) - 1;
+                mask &= mask - 1;
+                const int u = s0 >> 2;
+                const uint32_t bitpos = 4 * (lane & 7) + (s0 & 3);
+                const uint32_t word = u == 0 ? wv[0] : (u == 1 ? wv[1] : (u == 2 ? wv[2] : wv[3]));
+                const uint32_t woff = u == 0 ? wo[0] : (u == 1 ? wo[1] : (u == 2 ? wo[2] : wo[3]));
+                const uint64_t off = (uint64_t)tbase + woff + __popc(word & ((1u << bitpos) - 1u));
+                const uint32_t i = (uint32_t)e0 + slot_pos(s0, lane);
+                if (off < capacity) {
+                    float ev[(D > 0 ? D : kMaxRows)];
+                    gather<D>(ev, a.sketch, i, a.d, a.w, s_kh, s_ks);
+                    idx_out[off] = i;
+                    val_out[off] = a.scale * median_rows<D>(ev, a.d);
+                }
+            }
+        }
+        __syncthreads();  // s_task is rewritten by the next tile
+    }
+}
+
+template <int D>
+cudaError_t launch_dense_d(const DecodeArgs& a, float* out, cudaStream_t s) {
+    const uint64_t tasks = (a.n + kTaskElems - 1) / kTaskElems;
+    const uint64_t blocks = (tasks + (kThreads / 32) - 1) / (kThreads / 32);
+    decode_dense_kernel<D><<<grid_for(decode_dense_kernel<D>, blocks), kThreads, 0, s>>>(a, out);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_compact_write_d(const DecodeArgs& a, uint64_t tiles, const uint32_t* offsets,
+                                   uint32_t* idx_out, float* val_out, uint64_t capacity, cudaStream_t s) {
+    compact_write_kernel<D><<<grid_for(compact_write_kernel<D>, tiles), kThreads, 0, s>>>(
+        a, tiles, offsets, idx_out, val_out, capacity);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_dense(const DecodeArgs& a, float* out, cudaStream_t s) {
+    if (a.n == 0) return cudaSuccess;
+    switch (a.d) {
+        case 3: return launch_dense_d<3>(a, out, s);
+        case 5: return launch_dense_d<5>(a, out, s);
+        case 1: return launch_dense_d<1>(a, out, s);
+        default: return launch_dense_d<0>(a, out, s);
+    }
+}
+
+uint64_t compact_tiles(uint64_t nw) { return (nw + kCompactTileWords - 1) / kCompactTileWords; }
+
+size_t compact_workspace_bytes(uint64_t n) {
+    const uint64_t tiles = compact_tiles((n + 31) / 32);
+    const uint64_t one = (tiles * sizeof(uint32_t) + 255) / 256 * 256;
+    return (size_t)(2 * one);
+}
+
+cudaError_t launch_decode_compact(const DecodeArgs& a, uint32_t* idx_out, float* val_out, uint64_t capacity,
+                                  unsigned long long* count_out, uint32_t* tile_counts, uint32_t* tile_offsets,
+                                  cudaStream_t s) {
+    const uint64_t tiles = compact_tiles(a.nw);
+    if (tiles > 0) {
+        compact_count_kernel<<<grid_for(compact_count_kernel, tiles), kThreads, 0, s>>>(a.bitmap, a.nw, a.n,
+                                                                                        tiles, tile_counts);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    compact_scan_kernel<<<1, kScanThreads, 0, s>>>(tile_counts, tiles, tile_offsets, count_out);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || tiles == 0) return e;
+    switch (a.d) {
+        case 3: return launch_compact_write_d<3>(a, tiles, tile_offsets, idx_out, val_out, capacity, s);
+        case 5: return launch_compact_write_d<5>(a, tiles, tile_offsets, idx_out, val_out, capacity, s);
+        case 1: return launch_compact_write_d<1>(a, tiles, tile_offsets, idx_out, val_out, capacity, s);
+        default: return launch_compact_write_d<0>(a, tiles, tile_offsets, idx_out, val_out, capacity, s);
+    }
+}
+
+// ---- hash check --------------------------------------------------------------
+
+namespace {
+__global__ void __launch_bounds__(kThreads) hash_kernel(const uint32_t* __restrict__ idx, uint64_t m, uint32_t d,
+                                                        uint32_t w, RowKeys keys, uint32_t* __restrict__ bucket_out,
+                                                        int8_t* __restrict__ sign_out) {
+    const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t t = tid; t < m; t += stride) {
+        const uint32_t i = idx[t];
+        for (uint32_t j = 0; j < d; ++j) {
+            bucket_out[(uint64_t)j * m + t] = bucket_of(i, keys.kh[j], w);
+            sign_out[(uint64_t)j * m + t] = signbit_of(i, keys.ks[j]) ? (int8_t)-1 : (int8_t)1;
+        }
+    }
+}
+}  // namespace
+
+cudaError_t launch_hash(const uint32_t* idx, uint64_t m, uint32_t d, uint32_t w, RowKeys keys,
+                        uint32_t* bucket_out, int8_t* sign_out, cudaStream_t s) {
+    if (m == 0) return cudaSuccess;
+    const uint64_t blocks = (m + kThreads - 1) / kThreads;
+    hash_kernel<<<grid_for(hash_kernel, blocks), kThreads, 0, s>>>(idx, m, d, w, keys, bucket_out, sign_out);
+    return cudaGetLastError();
+}
+
+}  // namespace s2

@@ -1,0 +1,94 @@
+// Host-side launchers shared between the translation units of libs2.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "s2_device.cuh"
+
+namespace s2 {
+
+// A warp task covers 512 consecutive positions of one worker: 16 bitmap
+// words. Each lane owns 16 of the positions ("slots").
+constexpr int kTaskElems = 512;
+constexpr int kTaskWords = 16;
+constexpr int kThreads = 256;
+
+struct DeviceInfo {
+    int sms;
+    int l2_bytes;
+};
+cudaError_t device_info(DeviceInfo* out);
+
+// Keys of rows 0..d-1 for a seed (rows >= d are zero).
+RowKeys make_keys(uint32_t seed, uint32_t d);
+
+// ---- encode ----------------------------------------------------------------
+struct EncodeArgs {
+    const void* grad;   // first worker of the group
+    uint32_t* bitmaps;  // first worker of the group, [G][nw]
+    float* sketches;    // first worker of the group, [G][d*w]
+    uint64_t n;         // positions per worker
+    uint64_t nw;        // bitmap words per worker
+    uint64_t dw;        // d * w
+    uint32_t workers;   // G, workers in this launch
+    uint32_t tasks_per_worker;
+    uint32_t d;
+    uint32_t w;
+    RowKeys keys;
+};
+
+// dtype: 0 = f32, 1 = bf16. vec: rows are 16-byte aligned (vector loads).
+cudaError_t launch_encode(const EncodeArgs& a, int dtype, bool vec, cudaStream_t s);
+cudaError_t launch_zero(float* p, uint64_t count, cudaStream_t s);
+
+// ---- reduce ----------------------------------------------------------------
+cudaError_t launch_reduce(const uint32_t* bitmaps, const float* sketches, uint32_t W, uint64_t nw,
+                          uint64_t dw, uint32_t* bitmap_out, float* sketch_out, cudaStream_t s);
+
+// ---- decode ----------------------------------------------------------------
+struct DecodeArgs {
+    const uint32_t* bitmap;
+    const float* sketch;
+    uint64_t n;
+    uint64_t nw;
+    uint32_t d;
+    uint32_t w;
+    float scale;
+    RowKeys keys;
+};
+cudaError_t launch_decode_dense(const DecodeArgs& a, float* out, cudaStream_t s);
+
+constexpr int kCompactTileWords = 256;  // 8192 positions per tile
+uint64_t compact_tiles(uint64_t nw);
+size_t compact_workspace_bytes(uint64_t n);
+cudaError_t launch_decode_compact(const DecodeArgs& a, uint32_t* idx_out, float* val_out,
+                                  uint64_t capacity, unsigned long long* count_out,
+                                  uint32_t* tile_counts, uint32_t* tile_offsets, cudaStream_t s);
+
+cudaError_t launch_hash(const uint32_t* idx, uint64_t m, uint32_t d, uint32_t w, RowKeys keys,
+                        uint32_t* bucket_out, int8_t* sign_out, cudaStream_t s);
+
+// Blocks to launch for a grid-stride kernel: a multiple of the SM count
+// (resident blocks per SM from the occupancy calculator), capped by the work.
+template <typename Kernel>
+int grid_for(Kernel k, uint64_t work_blocks, size_t smem = 0) {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    int per_sm = cached[dev];
+    if (per_sm == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, smem) != cudaSuccess ||
+            per_sm < 1)
+            per_sm = 1;
+        cached[dev] = per_sm;
+    }
+    DeviceInfo di{};
+    if (device_info(&di) != cudaSuccess) di.sms = 1;
+    uint64_t full = (uint64_t)di.sms * (uint64_t)per_sm;
+    if (work_blocks < 1) work_blocks = 1;
+    return (int)(work_blocks < full ? work_blocks : full);
+}
+
+}  // namespace s2
