@@ -4,9 +4,9 @@ Argument marshalling only: every function below checks the torch tensors it
 is given (device, dtype, contiguity, sizes), passes their device pointers and
 the current CUDA stream to the C ABI declared in ``include/s2.h``, and raises
 ``S2Error`` on a non-OK status. All computation happens in the CUDA kernels
-of ``libs2.so``; there is no fallback. If the library has not been built,
-importing this package raises ``ImportError`` (build it with
-``python -m sketch_compressed_sparse_gb300.build``).
+of ``libs2.so``; there is no fallback. The library is loaded when this
+package is imported if it has been built; otherwise the first call raises
+``ImportError`` (build it with ``python -m sketch_compressed_sparse_gb300.build``).
 
 PyTorch is used for device memory and streams only.
 """
@@ -40,14 +40,6 @@ __all__ = [
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_lib", "libs2.so")
 
-if not os.path.exists(_LIB_PATH):
-    raise ImportError(
-        f"libs2.so not found at {_LIB_PATH}: build the CUDA library first "
-        "(python -m sketch_compressed_sparse_gb300.build)"
-    )
-
-_lib = ctypes.CDLL(_LIB_PATH)
-
 S2_OK, S2_ERR_INVALID_ARG, S2_ERR_ALIGNMENT, S2_ERR_UNSUPPORTED, S2_ERR_CUDA = range(5)
 S2_F32, S2_BF16 = 0, 1
 
@@ -59,43 +51,61 @@ class Params(ctypes.Structure):
 _u32, _u64, _i32, _f32, _vp, _sz = (ctypes.c_uint32, ctypes.c_uint64, ctypes.c_int, ctypes.c_float,
                                      ctypes.c_void_p, ctypes.c_size_t)
 
+_SIGS = {
+    "s2_encode": ([_vp, _i32, _u64, Params, _vp, _vp, _vp], _i32),
+    "s2_encode_batched": ([_vp, _i32, _u32, _u64, Params, _vp, _vp, _vp], _i32),
+    "s2_reduce": ([_vp, _vp, _u32, _u64, Params, _vp, _vp, _vp], _i32),
+    "s2_decode_dense": ([_vp, _vp, _u64, Params, _f32, _vp, _vp], _i32),
+    "s2_decode_workspace_size": ([_u64, ctypes.POINTER(_sz)], _i32),
+    "s2_decode_compact": ([_vp, _vp, _u64, Params, _f32, _vp, _vp, _u64, _vp, _vp, _sz, _vp], _i32),
+    "s2_hash": ([_vp, _u64, Params, _vp, _vp, _vp], _i32),
+    "s2_pipeline_workspace_size": ([_i32, _u32, _u64, Params, ctypes.POINTER(_sz)], _i32),
+    "s2_pipeline_dense_host": ([_vp, _i32, _u32, _u64, Params, _f32, _vp, _vp, _sz, _vp], _i32),
+    "s2_status_string": ([_i32], ctypes.c_char_p),
+    "s2_version": ([], ctypes.c_char_p),
+}
+_fns = {}
 
-def _sig(name, args, res=_i32):
-    f = getattr(_lib, name)
-    f.argtypes = args
-    f.restype = res
-    return f
+
+def _load():
+    """Load libs2.so once; raise ImportError if it has not been built."""
+    if _fns:
+        return _fns
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(
+            f"libs2.so not found at {_LIB_PATH}: build the CUDA library first "
+            "(python -m sketch_compressed_sparse_gb300.build)")
+    lib = ctypes.CDLL(_LIB_PATH)
+    for name, (args, res) in _SIGS.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+        _fns[name] = f
+    return _fns
 
 
-_enc = _sig("s2_encode", [_vp, _i32, _u64, Params, _vp, _vp, _vp])
-_encb = _sig("s2_encode_batched", [_vp, _i32, _u32, _u64, Params, _vp, _vp, _vp])
-_red = _sig("s2_reduce", [_vp, _vp, _u32, _u64, Params, _vp, _vp, _vp])
-_decd = _sig("s2_decode_dense", [_vp, _vp, _u64, Params, _f32, _vp, _vp])
-_decws = _sig("s2_decode_workspace_size", [_u64, ctypes.POINTER(_sz)])
-_decc = _sig("s2_decode_compact", [_vp, _vp, _u64, Params, _f32, _vp, _vp, _u64, _vp, _vp, _sz, _vp])
-_hash = _sig("s2_hash", [_vp, _u64, Params, _vp, _vp, _vp])
-_pws = _sig("s2_pipeline_workspace_size", [_i32, _u32, _u64, Params, ctypes.POINTER(_sz)])
-_pipe = _sig("s2_pipeline_dense_host", [_vp, _i32, _u32, _u64, Params, _f32, _vp, _vp, _sz, _vp])
-_stat = _sig("s2_status_string", [_i32], ctypes.c_char_p)
-_ver = _sig("s2_version", [], ctypes.c_char_p)
+def _f(name):
+    return (_fns or _load())[name]
 
 
 class S2Error(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {_stat(status).decode()} ({status})")
+        super().__init__(f"{where}: {s2_status_string(status)} ({status})")
 
 
 def lib_path() -> str:
+    """Path of the loaded libs2.so (loads it; ImportError if not built)."""
+    _load()
     return _LIB_PATH
 
 
 def s2_status_string(status: int) -> str:
-    return _stat(status).decode()
+    return _f("s2_status_string")(status).decode()
 
 
 def s2_version() -> str:
-    return _ver().decode()
+    return _f("s2_version")().decode()
 
 
 def nwords(n: int) -> int:
@@ -138,7 +148,7 @@ def s2_encode(grad: torch.Tensor, d: int, w: int, seed: int, bitmap: torch.Tenso
               stream=None) -> None:
     """One worker: grad [n] -> bitmap [nw] (int32 words), sketch [d, w] float32."""
     n = grad.numel()
-    _check(_enc(_dev(grad, "grad", _GRAD), _dtype_code(grad), n, Params(d, w, seed),
+    _check(_f("s2_encode")(_dev(grad, "grad", _GRAD), _dtype_code(grad), n, Params(d, w, seed),
                 _dev(bitmap, "bitmap", _U32, nwords(n)), _dev(sketch, "sketch", (torch.float32,), d * w),
                 _stream(stream)), "s2_encode")
 
@@ -149,7 +159,7 @@ def s2_encode_batched(grad: torch.Tensor, d: int, w: int, seed: int, bitmaps: to
     if grad.dim() != 2:
         raise ValueError("grad must be [W, n]")
     W, n = grad.shape
-    _check(_encb(_dev(grad, "grad", _GRAD), _dtype_code(grad), W, n, Params(d, w, seed),
+    _check(_f("s2_encode_batched")(_dev(grad, "grad", _GRAD), _dtype_code(grad), W, n, Params(d, w, seed),
                  _dev(bitmaps, "bitmaps", _U32, W * nwords(n)),
                  _dev(sketches, "sketches", (torch.float32,), W * d * w), _stream(stream)), "s2_encode_batched")
 
@@ -158,7 +168,7 @@ def s2_reduce(bitmaps: torch.Tensor, sketches: torch.Tensor, n: int, d: int, w: 
               sketch_out: torch.Tensor, stream=None) -> None:
     """bitmaps [W, nw], sketches [W, d, w] -> bitmap_out [nw] (OR), sketch_out [d, w] (sum)."""
     W = sketches.shape[0] if sketches.dim() == 3 else sketches.numel() // max(d * w, 1)
-    _check(_red(_dev(bitmaps, "bitmaps", _U32, W * nwords(n)),
+    _check(_f("s2_reduce")(_dev(bitmaps, "bitmaps", _U32, W * nwords(n)),
                 _dev(sketches, "sketches", (torch.float32,), W * d * w), W, n, Params(d, w, 0),
                 _dev(bitmap_out, "bitmap_out", _U32, nwords(n)),
                 _dev(sketch_out, "sketch_out", (torch.float32,), d * w), _stream(stream)), "s2_reduce")
@@ -167,14 +177,14 @@ def s2_reduce(bitmaps: torch.Tensor, sketches: torch.Tensor, n: int, d: int, w: 
 def s2_decode_dense(bitmap: torch.Tensor, sketch: torch.Tensor, n: int, d: int, w: int, seed: int,
                     out: torch.Tensor, scale: float = 1.0, stream=None) -> None:
     """bitmap [nw], sketch [d, w] -> out [n] float32 (median estimates, +0.0 at unset bits)."""
-    _check(_decd(_dev(bitmap, "bitmap", _U32, nwords(n)), _dev(sketch, "sketch", (torch.float32,), d * w), n,
+    _check(_f("s2_decode_dense")(_dev(bitmap, "bitmap", _U32, nwords(n)), _dev(sketch, "sketch", (torch.float32,), d * w), n,
                  Params(d, w, seed), scale, _dev(out, "out", (torch.float32,), n), _stream(stream)),
            "s2_decode_dense")
 
 
 def s2_decode_workspace_size(n: int) -> int:
     b = _sz()
-    _check(_decws(n, ctypes.byref(b)), "s2_decode_workspace_size")
+    _check(_f("s2_decode_workspace_size")(n, ctypes.byref(b)), "s2_decode_workspace_size")
     return int(b.value)
 
 
@@ -183,7 +193,7 @@ def s2_decode_compact(bitmap: torch.Tensor, sketch: torch.Tensor, n: int, d: int
                       workspace: torch.Tensor, scale: float = 1.0, stream=None) -> None:
     """bitmap, sketch -> idx_out [cap] int32, val_out [cap] float32, count_out [1] int64 (device)."""
     cap = min(idx_out.numel(), val_out.numel())
-    _check(_decc(_dev(bitmap, "bitmap", _U32, nwords(n)), _dev(sketch, "sketch", (torch.float32,), d * w), n,
+    _check(_f("s2_decode_compact")(_dev(bitmap, "bitmap", _U32, nwords(n)), _dev(sketch, "sketch", (torch.float32,), d * w), n,
                  Params(d, w, seed), scale, _dev(idx_out, "idx_out", _U32), _dev(val_out, "val_out", (torch.float32,)),
                  cap, _dev(count_out, "count_out", (torch.int64,), 1), _dev(workspace, "workspace", (torch.uint8,)),
                  workspace.numel(), _stream(stream)), "s2_decode_compact")
@@ -193,13 +203,13 @@ def s2_hash(idx: torch.Tensor, d: int, w: int, seed: int, bucket_out: torch.Tens
             stream=None) -> None:
     """idx [m] -> bucket_out [d, m] int32, sign_out [d, m] int8."""
     m = idx.numel()
-    _check(_hash(_dev(idx, "idx", _U32), m, Params(d, w, seed), _dev(bucket_out, "bucket_out", _U32, d * m),
+    _check(_f("s2_hash")(_dev(idx, "idx", _U32), m, Params(d, w, seed), _dev(bucket_out, "bucket_out", _U32, d * m),
                  _dev(sign_out, "sign_out", (torch.int8,), d * m), _stream(stream)), "s2_hash")
 
 
 def s2_pipeline_workspace_size(dtype: torch.dtype, W: int, n: int, d: int, w: int) -> int:
     b = _sz()
-    _check(_pws(S2_F32 if dtype == torch.float32 else S2_BF16, W, n, Params(d, w, 0), ctypes.byref(b)),
+    _check(_f("s2_pipeline_workspace_size")(S2_F32 if dtype == torch.float32 else S2_BF16, W, n, Params(d, w, 0), ctypes.byref(b)),
            "s2_pipeline_workspace_size")
     return int(b.value)
 
@@ -214,7 +224,7 @@ def s2_pipeline_dense_host(host_grad: torch.Tensor, d: int, w: int, seed: int, h
     W, n = host_grad.shape
     if host_out.dtype != torch.float32 or host_out.numel() < n or not host_out.is_contiguous():
         raise ValueError("host_out must be a contiguous float32 tensor of n elements")
-    _check(_pipe(host_grad.data_ptr(), _dtype_code(host_grad), W, n, Params(d, w, seed), scale,
+    _check(_f("s2_pipeline_dense_host")(host_grad.data_ptr(), _dtype_code(host_grad), W, n, Params(d, w, seed), scale,
                  host_out.data_ptr(), _dev(workspace, "workspace", (torch.uint8,)), workspace.numel(),
                  _stream(stream)), "s2_pipeline_dense_host")
 
@@ -224,3 +234,7 @@ def s2_pipeline_dense_host(host_grad: torch.Tensor, d: int, w: int, seed: int, h
 def alloc_encode_outputs(W: int, n: int, d: int, w: int, device="cuda") -> Tuple[torch.Tensor, torch.Tensor]:
     return (torch.empty((W, nwords(n)), dtype=torch.int32, device=device),
             torch.empty((W, d, w), dtype=torch.float32, device=device))
+
+
+if os.path.exists(_LIB_PATH):
+    _load()
