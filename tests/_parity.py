@@ -107,6 +107,7 @@ def gpu_pipeline(grad: torch.Tensor, d: int, w: int, seed: int, scale: float = 1
 def check_pipeline(host_grad: np.ndarray, dtype: str, got: dict, d: int, w: int, seed: int, scale: float = 1.0,
                    exact: bool = False):
     """Compare a gpu_pipeline result with the oracle on the same gradient."""
+    scale = float(np.float32(scale))  # the C ABI takes the scale as a float32
     ref = oracle.pipeline(host_grad, d, w, seed, dtype=dtype, scale=scale)
     n = host_grad.shape[1]
     np.testing.assert_array_equal(got["bitmaps"], ref["bitmaps"])

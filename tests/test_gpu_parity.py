@@ -125,7 +125,7 @@ def test_single_worker_encode_matches_batched_row():
     s2.s2_encode_batched(g, 5, 321, 0, bitmaps, sketches)
     bm1 = torch.empty(s2.nwords(wl.n), dtype=torch.int32, device=DEV)
     sk1 = torch.empty((5, 321), dtype=torch.float32, device=DEV)
-    s2.s2_encode(g[1].contiguous(), 5, 321, 0, bm1, sk1)
+    s2.s2_encode(g[1].clone(), 5, 321, 0, bm1, sk1)  # a fresh, 16-byte aligned row
     torch.cuda.synchronize()
     np.testing.assert_array_equal(u32(bm1), u32(bitmaps[1]))
     ref_bm, ref_S, ref_A = oracle.encode(wl.dense()[1], 5, 321, 0)
@@ -192,13 +192,14 @@ def test_decode_parity_on_planted_sketches(d, scale):
     cnt = torch.empty(1, dtype=torch.int64, device=DEV)
     s2.s2_decode_compact(tb, ts, n, d, w, seed, idx, val, cnt, ws, scale=scale)
     torch.cuda.synchronize()
-    want, _ = oracle.decode_dense(B, S.astype(np.float64), n, seed, scale)
+    scale32 = float(np.float32(scale))  # the C ABI takes the scale as a float32
+    want, _ = oracle.decode_dense(B, S.astype(np.float64), n, seed, scale32)
     got = out.cpu().numpy()
     if d % 2 == 1 or scale == 1.0:
         np.testing.assert_array_equal(got, want)
     else:
         np.testing.assert_allclose(got, want, rtol=2 ** -22, atol=0)
-    c, ridx, rval, _ = oracle.decode_compact(B, S.astype(np.float64), n, seed, scale)
+    c, ridx, rval, _ = oracle.decode_compact(B, S.astype(np.float64), n, seed, scale32)
     assert int(cnt.item()) == c
     np.testing.assert_array_equal(u32(idx[:c]), ridx)
     np.testing.assert_array_equal(val[:c].cpu().numpy(), got[ridx])
@@ -273,8 +274,9 @@ def test_alignment_and_overlap_errors():
     g = torch.zeros((2, 1024), dtype=torch.float32, device=DEV)
     bm = torch.empty((2, 32), dtype=torch.int32, device=DEV)
     sk = torch.empty((2, 3, 64), dtype=torch.float32, device=DEV)
+    big = torch.zeros(4096, dtype=torch.float32, device=DEV)
     with pytest.raises(s2.S2Error) as e:
-        s2.s2_encode_batched(g.view(-1)[1:2049].view(2, 1024), 3, 64, 0, bm, sk)
+        s2.s2_encode_batched(big[1:2049].view(2, 1024), 3, 64, 0, bm, sk)  # base 4 bytes past alignment
     assert e.value.status == 2  # alignment
     with pytest.raises(s2.S2Error) as e:
         s2.s2_encode_batched(g, 3, 64, 0, bm, g.view(-1)[:384].view(2, 3, 64))
