@@ -174,6 +174,16 @@ S2_API s2_status s2_pipeline_dense_host(const void *host_grad, s2_dtype dt, uint
                                  s2_params p, float scale, float *host_out, void *workspace,
                                  size_t workspace_bytes, s2_stream_t stream);
 
+/*
+ * s2_take_device_fault -- read and clear this device's fault word.
+ *   Kernels that wait on their own asynchronous copies bound every wait; if a
+ *   wait ever gives up, the kernel records a nonzero code here and returns
+ *   early, so the outputs of the calls since the last check are not valid.
+ *   *fault_out receives the code (0 = no fault). Synchronises with the device
+ *   (it reads device memory); call it between steps, not inside a hot loop.
+ */
+S2_API s2_status s2_take_device_fault(uint32_t *fault_out);
+
 /* Human-readable name of a status code (static string). */
 S2_API const char *s2_status_string(s2_status st);
 

@@ -4,9 +4,9 @@ Argument marshalling only: every function below checks the torch tensors it
 is given (device, dtype, contiguity, sizes), passes their device pointers and
 the current CUDA stream to the C ABI declared in ``include/s2.h``, and raises
 ``S2Error`` on a non-OK status. All computation happens in the CUDA kernels
-of ``libs2.so``; there is no fallback. The library is loaded when this
-package is imported if it has been built; otherwise the first call raises
-``ImportError`` (build it with ``python -m sketch_compressed_sparse_gb300.build``).
+of ``libs2.so``; there is no fallback. The library is loaded by the first
+call; if it has not been built that call raises ``ImportError`` (build it
+with ``python -m sketch_compressed_sparse_gb300.build``).
 
 PyTorch is used for device memory and streams only.
 """
@@ -32,6 +32,7 @@ __all__ = [
     "s2_pipeline_workspace_size",
     "s2_pipeline_dense_host",
     "s2_status_string",
+    "s2_take_device_fault",
     "s2_version",
     "S2_F32",
     "S2_BF16",
@@ -61,6 +62,7 @@ _SIGS = {
     "s2_hash": ([_vp, _u64, Params, _vp, _vp, _vp], _i32),
     "s2_pipeline_workspace_size": ([_i32, _u32, _u64, Params, ctypes.POINTER(_sz)], _i32),
     "s2_pipeline_dense_host": ([_vp, _i32, _u32, _u64, Params, _f32, _vp, _vp, _sz, _vp], _i32),
+    "s2_take_device_fault": ([ctypes.POINTER(_u32)], _i32),
     "s2_status_string": ([_i32], ctypes.c_char_p),
     "s2_version": ([], ctypes.c_char_p),
 }
@@ -106,6 +108,13 @@ def s2_status_string(status: int) -> str:
 
 def s2_version() -> str:
     return _f("s2_version")().decode()
+
+
+def s2_take_device_fault() -> int:
+    """Read and clear the device fault word (0 = every bounded wait completed)."""
+    v = _u32()
+    _check(_f("s2_take_device_fault")(ctypes.byref(v)), "s2_take_device_fault")
+    return int(v.value)
 
 
 def nwords(n: int) -> int:
@@ -234,7 +243,3 @@ def s2_pipeline_dense_host(host_grad: torch.Tensor, d: int, w: int, seed: int, h
 def alloc_encode_outputs(W: int, n: int, d: int, w: int, device="cuda") -> Tuple[torch.Tensor, torch.Tensor]:
     return (torch.empty((W, nwords(n)), dtype=torch.int32, device=device),
             torch.empty((W, d, w), dtype=torch.float32, device=device))
-
-
-if os.path.exists(_LIB_PATH):
-    _load()

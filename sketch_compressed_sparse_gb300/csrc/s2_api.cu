@@ -4,7 +4,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/s2.h"
+#include "s2.h"  // include/ is on the include path
 #include "s2_internal.h"
 
 namespace s2 {
@@ -342,6 +342,14 @@ s2_status s2_pipeline_dense_host(const void* host_grad, s2_dtype dt, uint32_t W,
     st = s2_decode_dense(d_bitmap, d_sketch, n, p, scale, d_out, stream);
     if (st != S2_OK) return st;
     if (cudaMemcpyAsync(host_out, d_out, (size_t)n * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess) return S2_ERR_CUDA;
+    return S2_OK;
+}
+
+s2_status s2_take_device_fault(uint32_t* fault_out) {
+    if (!fault_out) return S2_ERR_INVALID_ARG;
+    unsigned int v = 0;
+    if (take_encode_fault(&v) != cudaSuccess) return S2_ERR_CUDA;
+    *fault_out = v;
     return S2_OK;
 }
 

@@ -7,9 +7,11 @@
 // 0..15 load the words; every lane then owns 16 positions (4 chunks of 4
 // consecutive positions, so the dense output leaves as 16-byte streaming
 // stores). A lane walks only its set positions, two per step so that 2*d
-// independent gathers from the L2-resident sketch are in flight, and keeps
-// the results in registers. Unset positions are written as +0.0f with the
-// same stores.
+// independent gathers are in flight, and keeps the results in registers.
+// Unset positions are written as +0.0f with the same stores. The summed
+// sketch is gathered with an evict-last L2 policy so that the output stream
+// does not push it out of L2 (for a sketch of tens of MB this decides
+// between L2 hits and scattered DRAM reads).
 //
 // The compacted output uses three kernels and no inter-block waiting:
 // per-tile popcounts, one block that scans the tile totals (and writes the
@@ -26,23 +28,6 @@ __device__ __forceinline__ void load_keys(const RowKeys& k, uint32_t* s_kh, uint
         s_ks[threadIdx.x] = k.ks[threadIdx.x];
     }
     __syncthreads();
-}
-
-// Load the d signed estimates of position i.
-template <int D>
-__device__ __forceinline__ void gather(float (&e)[(D > 0 ? D : kMaxRows)], const float* __restrict__ sk,
-                                       uint32_t i, int d, uint32_t w, const uint32_t* s_kh,
-                                       const uint32_t* s_ks) {
-#pragma unroll
-    for (int j = 0; j < (D > 0 ? D : kMaxRows); ++j) {
-        if (D > 0 || j < d) {
-            const uint32_t b = bucket_of(i, s_kh[j], w);
-            const uint32_t sb = signbit_of(i, s_ks[j]);
-            e[j] = apply_sign(__ldg(sk + (uint64_t)j * w + b), sb);
-        } else {
-            e[j] = 0.f;
-        }
-    }
 }
 
 // Bitmap word wi, with the bits at positions >= n cleared (0 past the end).
@@ -71,11 +56,36 @@ __device__ __forceinline__ uint32_t lane_mask(uint32_t my_word, int lane) {
     return mask;
 }
 
+// Load the d signed estimates of position i with an L2 policy for the sketch.
+template <int D>
+__device__ __forceinline__ void gather_hint(float (&e)[(D > 0 ? D : kMaxRows)], const float* __restrict__ sk,
+                                            uint32_t i, int d, uint32_t w, const uint32_t* s_kh,
+                                            const uint32_t* s_ks, uint64_t pol) {
+#pragma unroll
+    for (int j = 0; j < (D > 0 ? D : kMaxRows); ++j) {
+        if (D > 0 || j < d) {
+            const uint32_t b = bucket_of(i, s_kh[j], w);
+            e[j] = apply_sign(ld_gather_f32(sk + (uint64_t)j * w + b, pol), signbit_of(i, s_ks[j]));
+        } else {
+            e[j] = 0.f;
+        }
+    }
+}
+
+// Dense decode, one warp per task of 512 positions. Lanes 0..15 load the 16
+// bitmap words; every lane then owns 16 positions (4 chunks of 4 consecutive
+// positions) and walks only its set ones, kPop per step, so that kPop * d
+// independent gathers from the L2-resident sketch (evict-last policy) are in
+// flight; results stay in registers and the 16 positions leave as four
+// 16-byte streaming stores, +0.0f at unset positions.
+constexpr int kPop = 2;
+
 template <int D>
 __global__ void __launch_bounds__(kThreads) decode_dense_kernel(DecodeArgs a, float* __restrict__ out) {
     __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
     load_keys(a.keys, s_kh, s_ks);
     const int lane = threadIdx.x & 31;
+    const uint64_t keep = policy_evict_last();
     const uint64_t ntasks = (a.n + kTaskElems - 1) / kTaskElems;
     const uint64_t nwarps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
     for (uint64_t t = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < ntasks; t += nwarps) {
@@ -87,20 +97,23 @@ __global__ void __launch_bounds__(kThreads) decode_dense_kernel(DecodeArgs a, fl
 #pragma unroll
         for (int s = 0; s < 16; ++s) r[s] = 0.f;
         while (mask) {
-            const int s0 = __ffs(mask) - 1;
-            mask &= mask - 1;
-            const bool two = mask != 0;
-            const int s1 = two ? __ffs(mask) - 1 : s0;
-            if (two) mask &= mask - 1;
-            float e0v[(D > 0 ? D : kMaxRows)], e1v[(D > 0 ? D : kMaxRows)];
-            gather<D>(e0v, a.sketch, (uint32_t)e0 + slot_pos(s0, lane), a.d, a.w, s_kh, s_ks);
-            gather<D>(e1v, a.sketch, (uint32_t)e0 + slot_pos(s1, lane), a.d, a.w, s_kh, s_ks);
-            const float v0 = a.scale * median_rows<D>(e0v, a.d);
-            const float v1 = a.scale * median_rows<D>(e1v, a.d);
+            int sl[kPop];
+            bool ok[kPop];
 #pragma unroll
-            for (int s = 0; s < 16; ++s) {
-                r[s] = (s == s0) ? v0 : r[s];
-                r[s] = (two && s == s1) ? v1 : r[s];
+            for (int q = 0; q < kPop; ++q) {
+                ok[q] = mask != 0;
+                sl[q] = ok[q] ? __ffs(mask) - 1 : (q ? sl[0] : 0);
+                if (ok[q]) mask &= mask - 1;
+            }
+            float ev[kPop][(D > 0 ? D : kMaxRows)];
+#pragma unroll
+            for (int q = 0; q < kPop; ++q)
+                gather_hint<D>(ev[q], a.sketch, (uint32_t)e0 + slot_pos(sl[q], lane), a.d, a.w, s_kh, s_ks, keep);
+#pragma unroll
+            for (int q = 0; q < kPop; ++q) {
+                const float v = a.scale * median_rows<D>(ev[q], a.d);
+#pragma unroll
+                for (int s = 0; s < 16; ++s) r[s] = (ok[q] && s == sl[q]) ? v : r[s];
             }
         }
 #pragma unroll
@@ -197,6 +210,7 @@ __global__ void __launch_bounds__(kThreads)
     __shared__ uint32_t s_task[16];
     load_keys(a.keys, s_kh, s_ks);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint64_t keep = policy_evict_last();
     for (uint64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
         uint32_t words[2], excl[2], tot[2];
 #pragma unroll
@@ -244,7 +258,7 @@ __global__ void __launch_bounds__(kThreads)
                 const uint32_t i = (uint32_t)e0 + slot_pos(s0, lane);
                 if (off < capacity) {
                     float ev[(D > 0 ? D : kMaxRows)];
-                    gather<D>(ev, a.sketch, i, a.d, a.w, s_kh, s_ks);
+                    gather_hint<D>(ev, a.sketch, i, a.d, a.w, s_kh, s_ks, keep);
                     idx_out[off] = i;
                     val_out[off] = a.scale * median_rows<D>(ev, a.d);
                 }

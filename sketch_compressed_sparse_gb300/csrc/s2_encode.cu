@@ -24,20 +24,29 @@ __device__ __forceinline__ uint32_t pick16(const uint4 (&v)[4], int slot) {
     return c == 0 ? q.x : (c == 1 ? q.y : (c == 2 ? q.z : q.w));
 }
 
-// Insert value `val` of position `i` into every row of the sketch.
+// Insert value `val` of position `i` into every row of the sketch. The
+// reductions carry an evict-last L2 policy: the sketch being built must stay
+// in L2 while the gradient streams past it.
 template <int D>
 __device__ __forceinline__ void insert(float* __restrict__ sk, uint32_t i, float val, int d, uint32_t w,
-                                       const uint32_t* s_kh, const uint32_t* s_ks) {
+                                       const uint32_t* s_kh, const uint32_t* s_ks, uint64_t keep) {
     const int rows = D > 0 ? D : d;
 #pragma unroll
     for (int j = 0; j < (D > 0 ? D : kMaxRows); ++j) {
         if (D > 0 || j < rows) {
             uint32_t b = bucket_of(i, s_kh[j], w);
             uint32_t sb = signbit_of(i, s_ks[j]);
-            red_add_f32(sk + (uint64_t)j * w + b, apply_sign(val, sb));
+            red_add_f32_hint(sk + (uint64_t)j * w + b, apply_sign(val, sb), keep);
         }
     }
 }
+
+// Tuning switches (compile-time): prefetch the next task's vectors into
+// registers before processing the current one; route 16-byte aligned rows
+// through the bulk-copy kernel; mbarrier suspend-time hint in ns (0: none).
+constexpr bool kPrefetchNext = true;
+constexpr bool kUseBulk = false;
+constexpr uint32_t kSuspendNs = 0;
 
 __device__ __forceinline__ void load_keys(const RowKeys& k, uint32_t* s_kh, uint32_t* s_ks) {
     if (threadIdx.x < kMaxRows) {
@@ -51,11 +60,28 @@ __device__ __forceinline__ void load_keys(const RowKeys& k, uint32_t* s_kh, uint
 // Lane l loads positions u*128 + 4l .. +3 of the task for u = 0..3; slot
 // 4u + c is position u*128 + 4l + c. Word q of chunk u is made of the
 // nibbles of lanes 8q .. 8q+7.
+// Load the 4 vectors of lane `lane` for the fp32 task at e0 of row g.
+__device__ __forceinline__ void load_f32_task(uint4 (&v)[4], const float* g, uint64_t e0, uint64_t n, int lane) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const uint64_t e = e0 + u * 128 + lane * 4;
+        if (e + 4 <= n) {
+            v[u] = ld_stream_u4(g + e);
+        } else {
+            v[u] = make_uint4(0, 0, 0, 0);
+            if (e + 0 < n) v[u].x = ld_stream_u32(g + e + 0);
+            if (e + 1 < n) v[u].y = ld_stream_u32(g + e + 1);
+            if (e + 2 < n) v[u].z = ld_stream_u32(g + e + 2);
+        }
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads) encode_f32_vec(EncodeArgs a) {
     __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
     load_keys(a.keys, s_kh, s_ks);
     const int lane = threadIdx.x & 31;
+    const uint64_t keep = policy_evict_last();
     const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
     uint32_t k = 0;
     uint32_t local = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -63,22 +89,20 @@ __global__ void __launch_bounds__(kThreads) encode_f32_vec(EncodeArgs a) {
         local -= a.tasks_per_worker;
         ++k;
     }
+    const float* grad = reinterpret_cast<const float*>(a.grad);
+    uint4 v[4];
+    if (k < a.workers) load_f32_task(v, grad + (uint64_t)k * a.n, (uint64_t)local * kTaskElems, a.n, lane);
     for (; k < a.workers;) {
         const uint64_t e0 = (uint64_t)local * kTaskElems;
-        const float* g = reinterpret_cast<const float*>(a.grad) + (uint64_t)k * a.n;
-        uint4 v[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const uint64_t e = e0 + u * 128 + lane * 4;
-            if (e + 4 <= a.n) {
-                v[u] = ld_stream_u4(g + e);
-            } else {
-                v[u] = make_uint4(0, 0, 0, 0);
-                if (e + 0 < a.n) v[u].x = ld_stream_u32(g + e + 0);
-                if (e + 1 < a.n) v[u].y = ld_stream_u32(g + e + 1);
-                if (e + 2 < a.n) v[u].z = ld_stream_u32(g + e + 2);
-            }
+        // the warp's next task, whose loads go out before this task is processed
+        uint32_t nk = k, nlocal = local + nwarps;
+        while (nlocal >= a.tasks_per_worker && nk < a.workers) {
+            nlocal -= a.tasks_per_worker;
+            ++nk;
         }
+        uint4 nv[4];
+        if (kPrefetchNext && nk < a.workers)
+            load_f32_task(nv, grad + (uint64_t)nk * a.n, (uint64_t)nlocal * kTaskElems, a.n, lane);
         uint32_t mask = 0;
         uint32_t my_word = 0;
 #pragma unroll
@@ -102,12 +126,15 @@ __global__ void __launch_bounds__(kThreads) encode_f32_vec(EncodeArgs a) {
             const int slot = __ffs(mask) - 1;
             mask &= mask - 1;
             const uint32_t i = (uint32_t)(e0 + (slot >> 2) * 128 + lane * 4 + (slot & 3));
-            insert<D>(sk, i, __uint_as_float(pick16(v, slot)), a.d, a.w, s_kh, s_ks);
+            insert<D>(sk, i, __uint_as_float(pick16(v, slot)), a.d, a.w, s_kh, s_ks, keep);
         }
-        local += nwarps;
-        while (local >= a.tasks_per_worker && k < a.workers) {
-            local -= a.tasks_per_worker;
-            ++k;
+        k = nk;
+        local = nlocal;
+        if (kPrefetchNext) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = nv[u];
+        } else if (k < a.workers) {
+            load_f32_task(v, grad + (uint64_t)k * a.n, (uint64_t)local * kTaskElems, a.n, lane);
         }
     }
 }
@@ -121,6 +148,7 @@ __global__ void __launch_bounds__(kThreads) encode_bf16_vec(EncodeArgs a) {
     __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
     load_keys(a.keys, s_kh, s_ks);
     const int lane = threadIdx.x & 31;
+    const uint64_t keep = policy_evict_last();
     const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
     uint32_t k = 0;
     uint32_t local = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -176,7 +204,7 @@ __global__ void __launch_bounds__(kThreads) encode_bf16_vec(EncodeArgs a) {
             const uint32_t word = (c >> 1) == 0 ? q.x : ((c >> 1) == 1 ? q.y : ((c >> 1) == 2 ? q.z : q.w));
             const uint32_t bits = (c & 1) ? (word & 0xffff0000u) : (word << 16);
             const uint32_t i = (uint32_t)(e0 + (slot >> 3) * 256 + lane * 8 + c);
-            insert<D>(sk, i, __uint_as_float(bits), a.d, a.w, s_kh, s_ks);
+            insert<D>(sk, i, __uint_as_float(bits), a.d, a.w, s_kh, s_ks, keep);
         }
         local += nwarps;
         while (local >= a.tasks_per_worker && k < a.workers) {
@@ -194,6 +222,7 @@ __global__ void __launch_bounds__(kThreads) encode_scalar(EncodeArgs a) {
     __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
     load_keys(a.keys, s_kh, s_ks);
     const int lane = threadIdx.x & 31;
+    const uint64_t keep = policy_evict_last();
     const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
     uint32_t k = 0;
     uint32_t local = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -238,12 +267,197 @@ __global__ void __launch_bounds__(kThreads) encode_scalar(EncodeArgs a) {
 #pragma unroll
             for (int s = 1; s < 16; ++s) bits = (slot == s) ? x[s] : bits;
             const uint32_t i = (uint32_t)(e0 + slot * 32 + lane);
-            insert<D>(sk, i, __uint_as_float(bits), a.d, a.w, s_kh, s_ks);
+            insert<D>(sk, i, __uint_as_float(bits), a.d, a.w, s_kh, s_ks, keep);
         }
         local += nwarps;
         while (local >= a.tasks_per_worker && k < a.workers) {
             local -= a.tasks_per_worker;
             ++k;
+        }
+    }
+}
+
+// ---- 16-byte aligned rows: per-warp bulk-copy (TMA) pipeline -------------
+// Each warp owns a ring of kBulkStages shared-memory stages of 2 KB. Lane 0
+// keeps the warp's next tasks in flight with cp.async.bulk copies that
+// complete on one mbarrier per stage; the warp waits (bounded) for a stage,
+// reads it with conflict-free 16-byte shared loads, assembles and stores the
+// task's bitmap words, compacts the task's nonzero positions into a per-warp
+// list (a warp prefix sum over the words' popcounts), and then processes the
+// list 32 entries at a time: every lane takes one nonzero, re-reads its value
+// from the stage and issues its d sketch reductions. Work per task is thus
+// proportional to its nonzeros with all lanes busy, whether the nonzeros come
+// as whole rows or scattered. The gradient stream bypasses registers and the
+// load/store unit and stays in flight while the warp issues reductions.
+// Task = 2 KB of gradient: 512 fp32 (16 words) or 1024 bf16 (32 words).
+// fp32: lane l's 16-byte vector u holds positions u*128 + 4l + c;
+// bf16: lane l's vector u holds positions u*256 + 8l + c.
+constexpr int kBulkStages = 3;
+constexpr uint32_t kBulkTaskBytes = 2048;
+constexpr uint32_t kSpinLimit = 1u << 22;
+
+__device__ unsigned int g_fault = 0;  // set when a bounded wait gave up
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t it = 0; it < limit; ++it) {
+        uint32_t ok;
+        if (kSuspendNs) {
+            asm volatile(
+                "{\n\t.reg .pred p;\n\t"
+                "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                "selp.u32 %0, 1, 0, p;\n\t}"
+                : "=r"(ok)
+                : "r"(bar), "r"(parity), "r"(kSuspendNs)
+                : "memory");
+        } else {
+            asm volatile(
+                "{\n\t.reg .pred p;\n\t"
+                "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                "selp.u32 %0, 1, 0, p;\n\t}"
+                : "=r"(ok)
+                : "r"(bar), "r"(parity)
+                : "memory");
+        }
+        if (ok) return true;
+    }
+    return false;
+}
+
+// Lane 0 of a warp: start copying task t (2 KB of gradient, or the shorter
+// tail of a worker row) into stage s; the stage's mbarrier expects its bytes.
+template <uint32_t kEsz>
+__device__ __forceinline__ void bulk_issue(const EncodeArgs& a, uint32_t t, uint32_t total, uint32_t ring_s,
+                                           uint32_t bar_s, int s, uint64_t policy) {
+    if (t >= total) return;
+    constexpr uint32_t kTE = kBulkTaskBytes / kEsz;
+    const uint32_t k = t / a.tasks_per_worker, local = t - k * a.tasks_per_worker;
+    const uint64_t e0 = (uint64_t)local * kTE;
+    const uint64_t left = a.n - e0;
+    const uint32_t bytes = (uint32_t)((left < kTE ? left : kTE) * kEsz);  // a multiple of 16
+    const unsigned char* src = static_cast<const unsigned char*>(a.grad) + ((uint64_t)k * a.n + e0) * kEsz;
+    const uint32_t bar = bar_s + 8 * s;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+        ::"r"(ring_s + s * kBulkTaskBytes), "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads) encode_bulk(EncodeArgs a) {
+    constexpr uint32_t kEsz = BF16 ? 2u : 4u;
+    constexpr uint32_t kTE = kBulkTaskBytes / kEsz;  // positions per task
+    constexpr uint32_t kTW = kTE / 32;               // bitmap words per task
+    extern __shared__ __align__(128) unsigned char s_ring[];  // [warp][stage][2 KB]
+    __shared__ __align__(8) uint64_t s_bar[kThreads / 32][kBulkStages];
+    __shared__ uint16_t s_list[kThreads / 32][kTE];
+    __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
+    load_keys(a.keys, s_kh, s_ks);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+    const uint32_t gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint32_t tpw = a.tasks_per_worker;
+    const uint32_t total = a.workers * tpw;
+    const unsigned char* ring = s_ring + (size_t)warp * kBulkStages * kBulkTaskBytes;
+    uint16_t* list = s_list[warp];
+    const uint32_t ring_s = smem_addr(ring);
+    const uint32_t bar_s = smem_addr(&s_bar[warp][0]);
+    const uint64_t keep = policy_evict_last();
+    uint64_t stream_pol = 0;
+    if (lane == 0) {
+        stream_pol = policy_evict_first();
+        for (int s = 0; s < kBulkStages; ++s)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_s + 8 * s) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    if (lane == 0)
+        for (int s = 0; s < kBulkStages; ++s)
+            bulk_issue<kEsz>(a, gw + s * nwarps, total, ring_s, bar_s, s, stream_pol);
+    uint32_t i = 0;
+    for (uint32_t t = gw; t < total; t += nwarps, ++i) {
+        const int s = i % kBulkStages;
+        if (!mbar_wait(bar_s + 8 * s, (i / kBulkStages) & 1, kSpinLimit)) {
+            // the copy never landed: report, drain what is still in flight (bounded), leave
+            if (lane == 0) atomicOr(&g_fault, 1u);
+            for (int q = 1; q < kBulkStages; ++q)
+                mbar_wait(bar_s + 8 * ((s + q) % kBulkStages), ((i + q) / kBulkStages) & 1, 1u << 16);
+            return;
+        }
+        const uint32_t k = t / tpw, local = t - k * tpw;
+        const uint64_t e0 = (uint64_t)local * kTE;
+        const uint64_t left = a.n - e0;
+        const uint32_t cnt = (uint32_t)(left < kTE ? left : kTE);
+        const unsigned char* st = ring + s * kBulkTaskBytes;
+        // 1. nonzero bits of the lane's 4 vectors -> bitmap word `lane` of the task
+        uint32_t my_word = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint4 v = *reinterpret_cast<const uint4*>(st + u * 512 + lane * 16);
+            const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+            uint32_t bits = 0;
+            if (!BF16) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) bits |= (uint32_t)((q[c] & 0x7fffffffu) != 0) << c;
+                const int valid = (int)cnt - (u * 128 + lane * 4);
+                if (valid < 4) bits &= valid <= 0 ? 0u : ((1u << valid) - 1u);
+                uint32_t part = bits << (4 * (lane & 7));
+                part |= __shfl_xor_sync(kFull, part, 1);
+                part |= __shfl_xor_sync(kFull, part, 2);
+                part |= __shfl_xor_sync(kFull, part, 4);
+                const uint32_t got = __shfl_sync(kFull, part, (lane & 3) * 8);
+                if ((lane >> 2) == u) my_word = got;
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    bits |= (uint32_t)((q[c] & 0x7fffu) != 0) << (2 * c);
+                    bits |= (uint32_t)((q[c] & 0x7fff0000u) != 0) << (2 * c + 1);
+                }
+                const int valid = (int)cnt - (u * 256 + lane * 8);
+                if (valid < 8) bits &= valid <= 0 ? 0u : ((1u << valid) - 1u);
+                uint32_t part = bits << (8 * (lane & 3));
+                part |= __shfl_xor_sync(kFull, part, 1);
+                part |= __shfl_xor_sync(kFull, part, 2);
+                const uint32_t got = __shfl_sync(kFull, part, (lane & 7) * 4);
+                if ((lane >> 3) == u) my_word = got;
+            }
+        }
+        if (lane < (int)kTW) {
+            const uint64_t wi = (uint64_t)local * kTW + lane;
+            if (wi < a.nw) a.bitmaps[(uint64_t)k * a.nw + wi] = my_word;
+        }
+        // 2. compact the set positions of the task into the warp's list
+        uint32_t nnz;
+        uint32_t at = warp_exclusive_scan(__popc(my_word), lane, &nnz);
+        for (uint32_t m = my_word; m; m &= m - 1) list[at++] = (uint16_t)(lane * 32 + __ffs(m) - 1);
+        __syncwarp();
+        // 3. every lane inserts one nonzero per round
+        float* sk = a.sketches + (uint64_t)k * a.dw;
+        for (uint32_t r = lane; r < nnz; r += 32) {
+            const uint32_t p = list[r];
+            const uint32_t bits = BF16 ? (uint32_t)(*reinterpret_cast<const uint16_t*>(st + 2 * p)) << 16
+                                       : *reinterpret_cast<const uint32_t*>(st + 4 * p);
+            const float val = __uint_as_float(bits);
+            const uint32_t i = (uint32_t)(e0 + p);
+            const int rows = D > 0 ? D : a.d;
+#pragma unroll
+            for (int j = 0; j < (D > 0 ? D : kMaxRows); ++j) {
+                if (D > 0 || j < rows) {
+                    const uint32_t b = bucket_of(i, s_kh[j], a.w);
+                    red_add_f32_hint(sk + (uint64_t)j * a.w + b, apply_sign(val, signbit_of(i, s_ks[j])), keep);
+                }
+            }
+        }
+        // Every lane has consumed its reads of this stage and of the list
+        // (their values fed the reductions), so both may be overwritten.
+        __syncwarp();
+        if (lane == 0) {
+            const uint32_t nt = t + kBulkStages * nwarps;
+            if (nt > t) bulk_issue<kEsz>(a, nt, total, ring_s, bar_s, s, stream_pol);
         }
     }
 }
@@ -259,14 +473,41 @@ __global__ void __launch_bounds__(kThreads) zero_f32(float* __restrict__ p, uint
     float* body = p + head;
     const uint64_t n4 = (count - head) / 4;
     float4* p4 = reinterpret_cast<float4*>(body);
-    for (uint64_t x = tid; x < n4; x += stride) p4[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const uint64_t keep = policy_evict_last();  // the encode that follows updates these lines
+    for (uint64_t x = tid; x < n4; x += stride) st_f4_hint(p4 + x, make_float4(0.f, 0.f, 0.f, 0.f), keep);
     for (uint64_t x = head + n4 * 4 + tid; x < count; x += stride) p[x] = 0.f;
+}
+
+constexpr size_t kBulkSmem = (size_t)(kThreads / 32) * kBulkStages * kBulkTaskBytes;
+
+template <int D, bool BF16>
+cudaError_t launch_bulk(const EncodeArgs& a, uint64_t tasks, cudaStream_t s) {
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(encode_bulk<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kBulkSmem);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    const uint64_t blocks = (tasks + (kThreads / 32) - 1) / (kThreads / 32);
+    encode_bulk<D, BF16><<<grid_for(encode_bulk<D, BF16>, blocks, kBulkSmem), kThreads, kBulkSmem, s>>>(a);
+    return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_encode_d(const EncodeArgs& a, int dtype, bool vec, cudaStream_t s) {
     const uint64_t tasks = (uint64_t)a.workers * a.tasks_per_worker;
     const uint64_t blocks = (tasks + (kThreads / 32) - 1) / (kThreads / 32);
+    const uint64_t esz = dtype == 0 ? 4 : 2;
+    const bool rows_aligned = (a.n * esz) % 16 == 0;
+    if (kUseBulk && vec && rows_aligned) {
+        EncodeArgs b = a;  // bulk tasks are 2 KB of gradient
+        b.tasks_per_worker = (uint32_t)((a.n * esz + kBulkTaskBytes - 1) / kBulkTaskBytes);
+        const uint64_t btasks = (uint64_t)b.workers * b.tasks_per_worker;
+        return dtype == 0 ? launch_bulk<D, false>(b, btasks, s) : launch_bulk<D, true>(b, btasks, s);
+    }
     if (vec && dtype == 0) {
         encode_f32_vec<D><<<grid_for(encode_f32_vec<D>, blocks), kThreads, 0, s>>>(a);
     } else if (vec && dtype == 1) {
@@ -289,6 +530,14 @@ cudaError_t launch_encode(const EncodeArgs& a, int dtype, bool vec, cudaStream_t
         case 1: return launch_encode_d<1>(a, dtype, vec, s);
         default: return launch_encode_d<0>(a, dtype, vec, s);
     }
+}
+
+cudaError_t take_encode_fault(unsigned int* out) {
+    unsigned int v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_fault, sizeof(v));
+    if (e == cudaSuccess && v) e = cudaMemcpyToSymbol(g_fault, &zero, sizeof(zero));
+    *out = v;
+    return e;
 }
 
 cudaError_t launch_zero(float* p, uint64_t count, cudaStream_t s) {

@@ -42,6 +42,7 @@ struct EncodeArgs {
 // dtype: 0 = f32, 1 = bf16. vec: rows are 16-byte aligned (vector loads).
 cudaError_t launch_encode(const EncodeArgs& a, int dtype, bool vec, cudaStream_t s);
 cudaError_t launch_zero(float* p, uint64_t count, cudaStream_t s);
+cudaError_t take_encode_fault(unsigned int* out);
 
 // ---- reduce ----------------------------------------------------------------
 cudaError_t launch_reduce(const uint32_t* bitmaps, const float* sketches, uint32_t W, uint64_t nw,

@@ -7,8 +7,8 @@
 // Design: a pure streaming kernel. Each thread owns one 16-byte vector of
 // the output and reads the W inputs at that offset with streaming loads
 // (they are read once), summing in the fixed order k = 0..W-1, so the result
-// is deterministic. Outputs use default stores so that the decode that
-// follows finds them in L2. The sketch part and the bitmap part are two
+// is deterministic. The summed sketch is stored with an evict-last L2 policy
+// so that the decode that follows finds it in L2. The sketch part and the bitmap part are two
 // index ranges of one grid.
 #include "s2_internal.h"
 
@@ -30,6 +30,7 @@ __global__ void __launch_bounds__(kThreads)
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
     const uint64_t s_items = SVEC ? dw / 4 : dw;
     const uint64_t b_items = BVEC ? nw / 4 : nw;
+    const uint64_t keep = policy_evict_last();  // the decode gathers from this sketch next
     for (uint64_t x = tid; x < s_items + b_items; x += stride) {
         if (x < s_items) {
             if (SVEC) {
@@ -54,7 +55,7 @@ __global__ void __launch_bounds__(kThreads)
                     acc.z += t.z;
                     acc.w += t.w;
                 }
-                reinterpret_cast<float4*>(sketch_out)[x] = acc;
+                st_f4_hint(reinterpret_cast<float4*>(sketch_out) + x, acc, keep);
             } else {
                 float acc = 0.f;
                 for (uint32_t k = 0; k < W; ++k)

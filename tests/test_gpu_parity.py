@@ -55,6 +55,8 @@ PIPELINE_CASES = [
     ("f32_one_worker_tail", dict(W=1, n=1001, d=3, w=64, density=0.3, tag=103)),  # vector path + tail
     ("bf16_vec", dict(W=4, n=8192, d=5, w=512, density=0.05, dtype="bf16", tag=104)),
     ("bf16_scalar_rows", dict(W=2, n=7777, d=3, w=300, density=0.2, dtype="bf16", tag=105)),
+    ("bf16_one_worker_tail", dict(W=1, n=1003, d=5, w=128, density=0.3, dtype="bf16", tag=115)),
+    ("f32_bulk_tail", dict(W=3, n=2048 * 3 + 4 * 7, d=3, w=512, density=0.2, tag=116)),  # 2 KB tasks + tail
     ("d1", dict(W=2, n=5000, d=1, w=4096, density=0.02, tag=106)),
     ("d2_even", dict(W=2, n=5000, d=2, w=777, density=0.05, tag=107)),
     ("d4_even", dict(W=5, n=6000, d=4, w=333, density=0.05, tag=108)),
@@ -71,6 +73,7 @@ PIPELINE_CASES = [
 def test_pipeline_parity(name, kw):
     wl = workloads.tiny() if kw is None else workloads.custom(**kw)
     got = gpu_pipeline(_grad(wl), wl.d, wl.w, wl.seed, compact=True)
+    assert s2.s2_take_device_fault() == 0
     check_pipeline(wl.dense(), wl.dtype, got, wl.d, wl.w, wl.seed)
 
 
