@@ -149,6 +149,36 @@ S2_API s2_status s2_decode_compact(const uint32_t *bitmap, const float *sketch, 
                             s2_stream_t stream);
 
 /*
+ * s2_decode_compact_noalloc -- s2_decode_compact without a workspace argument.
+ *
+ * The paper has no counterpart to this call; it exists for callers that
+ * cannot allocate device memory for a workspace: code running where a
+ * framework owns every byte of device memory through its own pool and
+ * forbids side allocations, code on a latency-critical path where a
+ * cudaMalloc (which may synchronise the device) is not acceptable, and code
+ * that keeps no state between calls in which a workspace could live.
+ *
+ * Same arguments, results and errors as s2_decode_compact, minus the
+ * workspace. The scratch it needs (per-tile counts and offsets) is a fixed
+ * 1 MiB array inside the library, allocated once per GPU when the library's
+ * device code is first loaded there and held until the process exits; the
+ * call itself allocates nothing. It accepts n up to 2^30 positions and
+ * returns S2_ERR_UNSUPPORTED beyond that.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the one array: calls whose kernels can
+ *     overlap on the GPU (different streams without ordering between them)
+ *     race and corrupt each other's results. Order such calls, or use
+ *     s2_decode_compact with one workspace per stream.
+ *   - Nothing in the array needs clearing between calls: each call writes
+ *     every entry it later reads.
+ */
+S2_API s2_status s2_decode_compact_noalloc(const uint32_t *bitmap, const float *sketch, uint64_t n,
+                                           s2_params p, float scale, uint32_t *idx_out, float *val_out,
+                                           uint64_t capacity, uint64_t *count_out, s2_stream_t stream);
+
+/*
  * s2_hash -- the bucket and sign hashes of m given positions, for checking.
  *   idx [m] uint32 in; bucket_out [d][m] uint32 and sign_out [d][m] int8
  *   (+1 or -1) out, row-major by row j.

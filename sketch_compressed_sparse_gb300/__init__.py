@@ -28,6 +28,7 @@ __all__ = [
     "s2_decode_dense",
     "s2_decode_workspace_size",
     "s2_decode_compact",
+    "s2_decode_compact_noalloc",
     "s2_hash",
     "s2_pipeline_workspace_size",
     "s2_pipeline_dense_host",
@@ -59,6 +60,7 @@ _SIGS = {
     "s2_decode_dense": ([_vp, _vp, _u64, Params, _f32, _vp, _vp], _i32),
     "s2_decode_workspace_size": ([_u64, ctypes.POINTER(_sz)], _i32),
     "s2_decode_compact": ([_vp, _vp, _u64, Params, _f32, _vp, _vp, _u64, _vp, _vp, _sz, _vp], _i32),
+    "s2_decode_compact_noalloc": ([_vp, _vp, _u64, Params, _f32, _vp, _vp, _u64, _vp, _vp], _i32),
     "s2_hash": ([_vp, _u64, Params, _vp, _vp, _vp], _i32),
     "s2_pipeline_workspace_size": ([_i32, _u32, _u64, Params, ctypes.POINTER(_sz)], _i32),
     "s2_pipeline_dense_host": ([_vp, _i32, _u32, _u64, Params, _f32, _vp, _vp, _sz, _vp], _i32),
@@ -206,6 +208,21 @@ def s2_decode_compact(bitmap: torch.Tensor, sketch: torch.Tensor, n: int, d: int
                  Params(d, w, seed), scale, _dev(idx_out, "idx_out", _U32), _dev(val_out, "val_out", (torch.float32,)),
                  cap, _dev(count_out, "count_out", (torch.int64,), 1), _dev(workspace, "workspace", (torch.uint8,)),
                  workspace.numel(), _stream(stream)), "s2_decode_compact")
+
+
+def s2_decode_compact_noalloc(bitmap: torch.Tensor, sketch: torch.Tensor, n: int, d: int, w: int, seed: int,
+                              idx_out: torch.Tensor, val_out: torch.Tensor, count_out: torch.Tensor,
+                              scale: float = 1.0, stream=None) -> None:
+    """s2_decode_compact with the library's own scratch instead of a workspace (n <= 2^30).
+
+    For callers that cannot allocate a workspace; see include/s2.h for the
+    one-time set-up on a device and why overlapping calls must be avoided.
+    """
+    cap = min(idx_out.numel(), val_out.numel())
+    _check(_f("s2_decode_compact_noalloc")(
+        _dev(bitmap, "bitmap", _U32, nwords(n)), _dev(sketch, "sketch", (torch.float32,), d * w), n,
+        Params(d, w, seed), scale, _dev(idx_out, "idx_out", _U32), _dev(val_out, "val_out", (torch.float32,)),
+        cap, _dev(count_out, "count_out", (torch.int64,), 1), _stream(stream)), "s2_decode_compact_noalloc")
 
 
 def s2_hash(idx: torch.Tensor, d: int, w: int, seed: int, bucket_out: torch.Tensor, sign_out: torch.Tensor,

@@ -252,15 +252,17 @@ s2_status s2_decode_workspace_size(uint64_t n, size_t* bytes) {
     return S2_OK;
 }
 
-s2_status s2_decode_compact(const uint32_t* bitmap, const float* sketch, uint64_t n, s2_params p, float scale,
-                            uint32_t* idx_out, float* val_out, uint64_t capacity, uint64_t* count_out,
-                            void* workspace, size_t workspace_bytes, s2_stream_t stream) {
+}  // extern "C"
+
+namespace {
+// Argument checks shared by both compacted decodes (everything but the workspace).
+s2_status check_decode_compact(const uint32_t* bitmap, const float* sketch, uint64_t n, s2_params p,
+                               const uint32_t* idx_out, const float* val_out, uint64_t capacity,
+                               const uint64_t* count_out, const void* workspace, size_t ws_bytes) {
     s2_status st = check_params(p);
     if (st != S2_OK) return st;
     if (n > kMaxN) return S2_ERR_UNSUPPORTED;
     if (!count_out) return S2_ERR_INVALID_ARG;
-    const size_t need = compact_workspace_bytes(n);
-    if (workspace_bytes < need || (need > 0 && !workspace)) return S2_ERR_INVALID_ARG;
     if (n > 0 && (!bitmap || !sketch)) return S2_ERR_INVALID_ARG;
     if (capacity > 0 && (!idx_out || !val_out)) return S2_ERR_INVALID_ARG;
     if (!aligned(bitmap, 16) || !aligned(sketch, 16) || !aligned(workspace, 16) || !aligned(idx_out, 4) ||
@@ -269,17 +271,50 @@ s2_status s2_decode_compact(const uint32_t* bitmap, const float* sketch, uint64_
     const uint64_t nw = words_of(n), dw = (uint64_t)p.d * p.w, cap = capacity < n ? capacity : n;
     const void* ins[2] = {bitmap, sketch};
     const uint64_t insz[2] = {nw * 4, dw * 4};
-    void* outs[4] = {idx_out, val_out, count_out, workspace};
-    const uint64_t outsz[4] = {cap * 4, cap * 4, 8, need};
+    const void* outs[4] = {idx_out, val_out, count_out, workspace};
+    const uint64_t outsz[4] = {cap * 4, cap * 4, 8, ws_bytes};
     for (int i = 0; i < 2; ++i)
         for (int o = 0; o < 4; ++o)
             if (overlap(ins[i], insz[i], outs[o], outsz[o])) return S2_ERR_INVALID_ARG;
     for (int o = 0; o < 4; ++o)
         for (int q = o + 1; q < 4; ++q)
             if (overlap(outs[o], outsz[o], outs[q], outsz[q])) return S2_ERR_INVALID_ARG;
-    const uint64_t tiles = compact_tiles(nw);
+    return S2_OK;
+}
+}  // namespace
+
+extern "C" {
+
+s2_status s2_decode_compact(const uint32_t* bitmap, const float* sketch, uint64_t n, s2_params p, float scale,
+                            uint32_t* idx_out, float* val_out, uint64_t capacity, uint64_t* count_out,
+                            void* workspace, size_t workspace_bytes, s2_stream_t stream) {
+    if (n <= kMaxN) {
+        const size_t need = compact_workspace_bytes(n);
+        if (workspace_bytes < need || (need > 0 && !workspace)) {
+            s2_status st = check_params(p);
+            return st != S2_OK ? st : S2_ERR_INVALID_ARG;
+        }
+    }
+    s2_status st = check_decode_compact(bitmap, sketch, n, p, idx_out, val_out, capacity, count_out, workspace,
+                                        n <= kMaxN ? compact_workspace_bytes(n) : 0);
+    if (st != S2_OK) return st;
+    const uint64_t tiles = compact_tiles(words_of(n));
     uint32_t* counts = static_cast<uint32_t*>(workspace);
     uint32_t* offsets = counts + (round256(tiles * 4) / 4);
+    return cuda_status(launch_decode_compact(make_decode_args(bitmap, sketch, n, p, scale), idx_out, val_out, capacity,
+                                             reinterpret_cast<unsigned long long*>(count_out), counts, offsets,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+s2_status s2_decode_compact_noalloc(const uint32_t* bitmap, const float* sketch, uint64_t n, s2_params p, float scale,
+                                    uint32_t* idx_out, float* val_out, uint64_t capacity, uint64_t* count_out,
+                                    s2_stream_t stream) {
+    s2_status st = check_decode_compact(bitmap, sketch, n, p, idx_out, val_out, capacity, count_out, nullptr, 0);
+    if (st != S2_OK) return st;
+    if (n > noalloc_compact_max_n()) return S2_ERR_UNSUPPORTED;
+    uint32_t* counts = nullptr;
+    uint32_t* offsets = nullptr;
+    if (noalloc_compact_scratch(&counts, &offsets) != cudaSuccess) return S2_ERR_CUDA;
     return cuda_status(launch_decode_compact(make_decode_args(bitmap, sketch, n, p, scale), idx_out, val_out, capacity,
                                              reinterpret_cast<unsigned long long*>(count_out), counts, offsets,
                                              reinterpret_cast<cudaStream_t>(stream)));

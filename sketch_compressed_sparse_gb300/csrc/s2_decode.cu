@@ -17,6 +17,8 @@
 // per-tile popcounts, one block that scans the tile totals (and writes the
 // final count), and a writer that recomputes the in-tile offsets with warp
 // scans and writes (index, value) pairs in ascending order.
+#include <mutex>
+
 #include "s2_internal.h"
 
 namespace s2 {
@@ -323,6 +325,41 @@ cudaError_t launch_decode_compact(const DecodeArgs& a, uint32_t* idx_out, float*
         case 1: return launch_compact_write_d<1>(a, tiles, tile_offsets, idx_out, val_out, capacity, s);
         default: return launch_compact_write_d<0>(a, tiles, tile_offsets, idx_out, val_out, capacity, s);
     }
+}
+
+// ---- compaction with library-owned scratch -----------------------------------
+// s2_decode_compact_noalloc runs the same three kernels as s2_decode_compact,
+// but its tile counts and tile offsets live in this file-scope device array
+// instead of a caller workspace. It covers n up to kNoAllocMaxN positions
+// (2^30: 131,072 tiles, 1 MiB); every GPU that loads the library holds the
+// array until the process exits. Nothing in it has to start at zero: a call
+// writes every count it later scans and every offset it later reads.
+constexpr uint64_t kNoAllocMaxN = 1ull << 30;
+constexpr uint64_t kNoAllocMaxTiles = (kNoAllocMaxN / 32) / kCompactTileWords;
+static __device__ __align__(256) uint32_t g_noalloc_compact_scratch[2 * kNoAllocMaxTiles];
+
+uint64_t noalloc_compact_max_n() { return kNoAllocMaxN; }
+
+// Device address of the scratch for the current device. The address is looked
+// up once per device (cudaGetSymbolAddress with that device current) and
+// cached; host code must never pass the symbol itself to a kernel.
+cudaError_t noalloc_compact_scratch(uint32_t** counts, uint32_t** offsets) {
+    static std::once_flag once[64];
+    static uint32_t* base[64];
+    static cudaError_t status[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::call_once(once[dev], [dev] {
+        void* p = nullptr;
+        status[dev] = cudaGetSymbolAddress(&p, g_noalloc_compact_scratch);
+        base[dev] = static_cast<uint32_t*>(p);
+    });
+    if (status[dev] != cudaSuccess) return status[dev];
+    *counts = base[dev];
+    *offsets = base[dev] + kNoAllocMaxTiles;
+    return cudaSuccess;
 }
 
 // ---- hash check --------------------------------------------------------------

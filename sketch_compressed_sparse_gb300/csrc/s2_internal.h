@@ -68,6 +68,10 @@ cudaError_t launch_decode_compact(const DecodeArgs& a, uint32_t* idx_out, float*
                                   uint64_t capacity, unsigned long long* count_out,
                                   uint32_t* tile_counts, uint32_t* tile_offsets, cudaStream_t s);
 
+// Library-owned scratch of s2_decode_compact_noalloc (see s2_decode.cu).
+uint64_t noalloc_compact_max_n();
+cudaError_t noalloc_compact_scratch(uint32_t** counts, uint32_t** offsets);
+
 cudaError_t launch_hash(const uint32_t* idx, uint64_t m, uint32_t d, uint32_t w, RowKeys keys,
                         uint32_t* bucket_out, int8_t* sign_out, cudaStream_t s);
 

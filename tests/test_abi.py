@@ -128,6 +128,18 @@ def test_compact_workspace_and_errors(lib):
     assert call(args(val=A + 2**21 + 16)) == INVALID  # idx and val overlap
 
 
+def test_compact_noalloc_limits(lib):
+    dc = _fn(lib, "s2_decode_compact_noalloc", [VP, VP, U64, Params, F32, VP, VP, U64, VP, VP])
+    good = Params(3, 64, 0)
+    big = 2**34  # fake, far-apart addresses: nothing overlaps, nothing is dereferenced
+    call = lambda n, cnt=A + 4 * big: dc(A, A + big, n, good, 1.0, A + 2 * big, A + 3 * big, 16, cnt, None)
+    assert call((1 << 30) + 1) == UNSUP  # beyond the library-owned scratch
+    assert call(2**32) == UNSUP
+    assert call(1000, cnt=None) == INVALID
+    assert call(1000, cnt=A + 4 * big + 4) == ALIGN
+    assert dc(A, A + big, 1000, Params(0, 64, 0), 1.0, A + 2 * big, A + 3 * big, 16, A + 4 * big, None) == INVALID
+
+
 def test_hash_and_pipeline_errors(lib):
     h = _fn(lib, "s2_hash", [VP, U64, Params, VP, VP, VP])
     assert h(A, 10, Params(3, 0, 0), A + 4096, A + 8192, None) == INVALID
