@@ -62,6 +62,36 @@ def algorithmic_bytes(wl: workloads.Workload, nnz_union: int) -> dict:
     return {"encode": enc, "reduce": red, "decode": dec, "total": enc + red + dec}
 
 
+def l2_sector_ops(wl: workloads.Workload, nnz_union: int) -> dict:
+    """32-byte L2 sector operations each stage issues at minimum.
+
+    Streams count one operation per 32-byte sector; every scattered 4-byte
+    sketch reduction (encode) or gather (decode) is one operation of its own.
+    encode: read grad, write bitmaps, zero-fill and then update (W nnz d
+            reductions) the per-worker sketches;
+    reduce: read W bitmaps and sketches, write one of each;
+    decode: read the bitmap, d gathers per set position, write the output.
+    """
+    W, n, d, w = wl.W, wl.n, wl.d, wl.w
+    sec = lambda b: (b + 31) // 32
+    BM = 4 * ((n + 31) // 32)
+    SK = 4 * d * w
+    nnz = sum(wl.nnz_per_worker)
+    enc = sec(W * n * wl.elem_bytes) + W * sec(BM) + W * sec(SK) + nnz * d
+    red = W * (sec(SK) + sec(BM)) + sec(SK) + sec(BM)
+    dec = sec(BM) + nnz_union * d + sec(4 * n)
+    return {"encode": enc, "reduce": red, "decode": dec, "total": enc + red + dec}
+
+
+def measured_ceilings():
+    """Scattered-operation ceilings measured by `bench.py --ceilings` on this GPU model."""
+    p = os.path.join(ROOT, "profiles", "ceilings_gb300.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        return json.load(f)
+
+
 def encode_launches(wl: workloads.Workload, l2_bytes: int) -> int:
     """Kernels one s2_encode_batched call launches: a zero fill and an encode per
     group of workers whose sketches fit in 40% of L2 together."""
@@ -303,6 +333,15 @@ def run_ours(args, wl, world, rank, local):
         "gpu_launches": K * (n_enc + 2),
         "wall_ms_timed_region": round(wall * 1e3, 3),
     }
+    ops = l2_sector_ops(wl, nnz_u)
+    ceil = measured_ceilings()
+    step_s = total_ms / 1e3 / K
+    l2 = {"unit": "G sector ops/s", "ops_per_step": ops, "achieved": round(ops["total"] / step_s / 1e9, 1)}
+    if ceil:
+        c = float(ceil["red_f32"]["Gops_per_s"])
+        l2.update(peak=c, frac=round(ops["total"] / step_s / 1e9 / c, 4),
+                  peak_source="scattered red.f32 rate measured by bench.py --ceilings (profiles/ceilings_gb300.json)")
+    res["l2_roofline"] = l2
     res["clocks"] = clk.summary()
 
     if not args.no_e2e:
@@ -377,6 +416,32 @@ def run_reference(args, wl):
     }
 
 
+def select_workers(wl: workloads.Workload, k):
+    if k is None or k >= wl.W:
+        return wl
+    wl.W, wl.idx, wl.val = k, wl.idx[:k], wl.val[:k]
+    wl.name = f"{wl.name}_W{k}"
+    return wl
+
+
+def run_ceilings(args):
+    """Compile ceilings.cu for sm_103a and print its JSON line."""
+    import tempfile
+
+    from sketch_compressed_sparse_gb300 import build as b
+
+    with tempfile.TemporaryDirectory() as td:
+        exe = os.path.join(td, "ceilings")
+        subprocess.check_call([b.nvcc(), *b.ARCH, "-O3", "-o", exe, os.path.join(ROOT, "ceilings.cu")])
+        out = subprocess.run([exe], capture_output=True, text=True)
+    line = out.stdout.strip().splitlines()[-1] if out.stdout.strip() else json.dumps({"error": out.stderr[-500:]})
+    print(line, flush=True)
+    if args.out:
+        with open(args.out, "a") as f:
+            f.write(line + "\n")
+    return out.returncode
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -388,7 +453,13 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle timing")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
+    ap.add_argument("--workers", type=int, default=None,
+                    help="profiling aid: keep only the first K workers of the workload (changes the workload)")
+    ap.add_argument("--ceilings", action="store_true",
+                    help="build and run ceilings.cu (device ceilings of scattered L2 operations) and exit")
     args = ap.parse_args(argv)
+    if args.ceilings:
+        return run_ceilings(args)
     if args.warmup < 3 and args.impl == "ours" and args.steps > 5:
         ap.error("use at least 3 warm-up steps")
 
@@ -404,7 +475,7 @@ def main(argv=None):
 
             torch.cuda.set_device(local)
             dist.init_process_group("nccl")
-        res = run_ours(args, workloads.by_name(args.config), world, rank, local)
+        res = run_ours(args, select_workers(workloads.by_name(args.config), args.workers), world, rank, local)
         if world > 1:
             import torch.distributed as dist
 

@@ -26,6 +26,23 @@ def test_algorithmic_bytes_embedding():
     assert abs(by["total"] / 1e6 - 1029.2) < 0.1
 
 
+def test_l2_sector_ops_embedding():
+    wl = workloads.embedding()
+    ops = bench.l2_sector_ops(wl, wl.union_nnz())
+    nw = (wl.n + 31) // 32
+    assert ops["encode"] == 8 * wl.n * 4 // 32 + 8 * (nw * 4 // 32) + 8 * (5 * (1 << 20) * 4 // 32) + 8 * 1_024_000 * 5
+    assert ops["decode"] == nw * 4 // 32 + wl.union_nnz() * 5 + wl.n * 4 // 32
+    assert ops["total"] == ops["encode"] + ops["reduce"] + ops["decode"]
+
+
+def test_select_workers_keeps_a_prefix():
+    wl = workloads.custom(W=4, n=1000, d=3, w=64, density=0.1)
+    first = [a.copy() for a in wl.idx[:2]]
+    wl2 = bench.select_workers(wl, 2)
+    assert wl2.W == 2 and len(wl2.idx) == 2 and all((a == b).all() for a, b in zip(wl2.idx, first))
+    assert bench.select_workers(workloads.tiny(), None).W == 2
+
+
 def test_encode_launch_groups():
     wl = workloads.Workload("e", 8, 1000, 5, 1 << 20, 0, "f32", [], [])  # 20 MiB sketch per worker
     assert bench.encode_launches(wl, 126 << 20) == 2 * 4  # two workers per group
