@@ -62,6 +62,23 @@ def algorithmic_bytes(wl: workloads.Workload, nnz_union: int) -> dict:
     return {"encode": enc, "reduce": red, "decode": dec, "total": enc + red + dec}
 
 
+def algorithmic_bytes_fused(wl: workloads.Workload, nnz_union: int) -> dict:
+    """Fused single-sketch mode: read grad once, write the aggregate bitmap and
+    sketch once; the decode as in the per-worker path."""
+    by = algorithmic_bytes(wl, nnz_union)
+    BM = 4 * ((wl.n + 31) // 32)
+    SK = 4 * wl.d * wl.w
+    fused = wl.W * wl.n * wl.elem_bytes + BM + SK
+    return {"encode_reduce_fused": fused, "decode": by["decode"], "total": fused + by["decode"]}
+
+
+def l2_sector_ops_fused(wl: workloads.Workload, nnz_union: int) -> dict:
+    sec = lambda b: (b + 31) // 32
+    ops = l2_sector_ops(wl, nnz_union)
+    fused = sec(wl.W * wl.n * wl.elem_bytes) + sec(4 * ((wl.n + 31) // 32)) + sec(4 * wl.d * wl.w) + nnz_union * wl.d
+    return {"encode_reduce_fused": fused, "decode": ops["decode"], "total": fused + ops["decode"]}
+
+
 def l2_sector_ops(wl: workloads.Workload, nnz_union: int) -> dict:
     """32-byte L2 sector operations each stage issues at minimum.
 
@@ -246,16 +263,24 @@ def run_ours(args, wl, world, rank, local):
     W, n, d, w, seed = wl.W, wl.n, wl.d, wl.w, wl.seed
     nnz_u = wl.union_nnz()
     grad = wl.dense_torch(dev)
-    bitmaps, sketches = s2.alloc_encode_outputs(W, n, d, w, dev)
+    if args.mode == "fused":
+        bitmaps = sketches = None
+    else:
+        bitmaps, sketches = s2.alloc_encode_outputs(W, n, d, w, dev)
     bitmap = torch.empty(s2.nwords(n), dtype=torch.int32, device=dev)
     sketch = torch.empty((d, w), dtype=torch.float32, device=dev)
     out = torch.empty(n, dtype=torch.float32, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    fused = args.mode == "fused"
+
     def step():
-        s2.s2_encode_batched(grad, d, w, seed, bitmaps, sketches)
-        s2.s2_reduce(bitmaps, sketches, n, d, w, bitmap, sketch)
+        if fused:
+            s2.s2_encode_reduce_fused(grad, d, w, seed, bitmap, sketch)
+        else:
+            s2.s2_encode_batched(grad, d, w, seed, bitmaps, sketches)
+            s2.s2_reduce(bitmaps, sketches, n, d, w, bitmap, sketch)
         s2.s2_decode_dense(bitmap, sketch, n, d, w, seed, out)
 
     for _ in range(args.warmup):
@@ -276,9 +301,13 @@ def run_ours(args, wl, world, rank, local):
             flush.fill_(float(k & 7))
             e = ev[k]
             e[0].record(stream)
-            s2.s2_encode_batched(grad, d, w, seed, bitmaps, sketches)
-            e[1].record(stream)
-            s2.s2_reduce(bitmaps, sketches, n, d, w, bitmap, sketch)
+            if fused:
+                s2.s2_encode_reduce_fused(grad, d, w, seed, bitmap, sketch)
+                e[1].record(stream)
+            else:
+                s2.s2_encode_batched(grad, d, w, seed, bitmaps, sketches)
+                e[1].record(stream)
+                s2.s2_reduce(bitmaps, sketches, n, d, w, bitmap, sketch)
             e[2].record(stream)
             s2.s2_decode_dense(bitmap, sketch, n, d, w, seed, out)
             e[3].record(stream)
@@ -342,6 +371,27 @@ def run_ours(args, wl, world, rank, local):
         l2.update(peak=c, frac=round(ops["total"] / step_s / 1e9 / c, 4),
                   peak_source="scattered red.f32 rate measured by bench.py --ceilings (profiles/ceilings_gb300.json)")
     res["l2_roofline"] = l2
+    res["config"]["mode"] = "per_worker (encode_batched + reduce + decode_dense)"
+    if fused:
+        # same step with encode + reduce replaced by the fused single-sketch pass
+        byf = algorithmic_bytes_fused(wl, nnz_u)
+        fused_s = enc_ms / 1e3 / K
+        ach = byf["encode_reduce_fused"] / fused_s / 1e9
+        pg = byf["total"] / step_s / 1e9
+        res["config"]["mode"] = "fused_single_sketch (encode_reduce_fused + decode_dense)"
+        res["stages_ms_per_step"] = {"encode_reduce_fused": round(enc_ms / K, 5), "decode": round(dec_ms / K, 5)}
+        res["roofline"] = {"kernel": "encode_reduce_fused (zero fill + one pass over all workers)", "bound": "hbm",
+                           "achieved": round(ach, 1), "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
+                           "traffic": None, "algorithmic_bytes_per_step": byf["encode_reduce_fused"],
+                           "launches_per_step": 2, "peak_source": res["roofline"]["peak_source"]}
+        res["path_roofline"] = {"bound": "hbm", "achieved": round(pg, 1), "peak": peak, "unit": "GB/s",
+                                "frac": round(pg / peak, 4), "algorithmic_bytes_per_step": byf["total"]}
+        res["gpu_launches"] = K * 3
+        opsf = l2_sector_ops_fused(wl, nnz_u)
+        l2 = dict(l2, ops_per_step=opsf, achieved=round(opsf["total"] / step_s / 1e9, 1))
+        if ceil:
+            l2["frac"] = round(opsf["total"] / step_s / 1e9 / float(ceil["red_f32"]["Gops_per_s"]), 4)
+        res["l2_roofline"] = l2
     res["clocks"] = clk.summary()
 
     if not args.no_e2e:
@@ -453,6 +503,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle timing")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
+    ap.add_argument("--mode", choices=["per_worker", "fused"], default="per_worker",
+                    help="per_worker: the simulated data-parallel path (default); fused: encode_reduce_fused + decode")
     ap.add_argument("--workers", type=int, default=None,
                     help="profiling aid: keep only the first K workers of the workload (changes the workload)")
     ap.add_argument("--ceilings", action="store_true",

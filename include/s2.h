@@ -118,6 +118,25 @@ S2_API s2_status s2_reduce(const uint32_t *bitmaps, const float *sketches, uint3
                     s2_params p, uint32_t *bitmap_out, float *sketch_out, s2_stream_t stream);
 
 /*
+ * s2_encode_reduce_fused -- s2_encode_batched followed by s2_reduce in one
+ * pass, for workers that all live on this GPU (Section 3.1 "Collecting
+ * Sparse-Sketch with AllReduce": because the sketch is linear, the sum of the
+ * workers' sketches is the sketch of the summed gradient).
+ *   grad [W][n] in (16-byte aligned base, any n);
+ *   bitmap_out [nw] = OR over k of the workers' nonzero bitmaps (identical to
+ *   s2_reduce's output); sketch_out [d][w] = the summed sketch: the workers'
+ *   values are added per position (order k = 0..W-1) and each union position
+ *   is inserted once, so the result equals s2_reduce's up to float32
+ *   rounding order.
+ * The per-worker bitmaps and sketches (what each worker of a real
+ * distributed run would send into the AllReduce) are never formed, so this
+ * is a same-GPU shortcut, measured separately from the per-worker path.
+ * W = 0 writes a zero bitmap and sketch.
+ */
+S2_API s2_status s2_encode_reduce_fused(const void *grad, s2_dtype dt, uint32_t W, uint64_t n, s2_params p,
+                                        uint32_t *bitmap_out, float *sketch_out, s2_stream_t stream);
+
+/*
  * s2_decode_dense -- decompression phase with a dense output (Section 3.1
  * "Decompressing Sparse Gradient"; Algorithm 1, decompression loop).
  *   bitmap [nw], sketch [d][w] in; out [n] float32 (16-byte aligned).

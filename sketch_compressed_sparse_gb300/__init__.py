@@ -25,6 +25,7 @@ __all__ = [
     "s2_encode",
     "s2_encode_batched",
     "s2_reduce",
+    "s2_encode_reduce_fused",
     "s2_decode_dense",
     "s2_decode_workspace_size",
     "s2_decode_compact",
@@ -57,6 +58,7 @@ _SIGS = {
     "s2_encode": ([_vp, _i32, _u64, Params, _vp, _vp, _vp], _i32),
     "s2_encode_batched": ([_vp, _i32, _u32, _u64, Params, _vp, _vp, _vp], _i32),
     "s2_reduce": ([_vp, _vp, _u32, _u64, Params, _vp, _vp, _vp], _i32),
+    "s2_encode_reduce_fused": ([_vp, _i32, _u32, _u64, Params, _vp, _vp, _vp], _i32),
     "s2_decode_dense": ([_vp, _vp, _u64, Params, _f32, _vp, _vp], _i32),
     "s2_decode_workspace_size": ([_u64, ctypes.POINTER(_sz)], _i32),
     "s2_decode_compact": ([_vp, _vp, _u64, Params, _f32, _vp, _vp, _u64, _vp, _vp, _sz, _vp], _i32),
@@ -183,6 +185,18 @@ def s2_reduce(bitmaps: torch.Tensor, sketches: torch.Tensor, n: int, d: int, w: 
                 _dev(sketches, "sketches", (torch.float32,), W * d * w), W, n, Params(d, w, 0),
                 _dev(bitmap_out, "bitmap_out", _U32, nwords(n)),
                 _dev(sketch_out, "sketch_out", (torch.float32,), d * w), _stream(stream)), "s2_reduce")
+
+
+def s2_encode_reduce_fused(grad: torch.Tensor, d: int, w: int, seed: int, bitmap_out: torch.Tensor,
+                           sketch_out: torch.Tensor, stream=None) -> None:
+    """W resident workers in one pass: grad [W, n] -> aggregate bitmap [nw], summed sketch [d, w]."""
+    if grad.dim() != 2:
+        raise ValueError("grad must be [W, n]")
+    W, n = grad.shape
+    _check(_f("s2_encode_reduce_fused")(_dev(grad, "grad", _GRAD), _dtype_code(grad), W, n, Params(d, w, seed),
+                                        _dev(bitmap_out, "bitmap_out", _U32, nwords(n)),
+                                        _dev(sketch_out, "sketch_out", (torch.float32,), d * w), _stream(stream)),
+           "s2_encode_reduce_fused")
 
 
 def s2_decode_dense(bitmap: torch.Tensor, sketch: torch.Tensor, n: int, d: int, w: int, seed: int,

@@ -237,6 +237,33 @@ s2_status s2_reduce(const uint32_t* bitmaps, const float* sketches, uint32_t W, 
     return cuda_status(launch_reduce(bitmaps, sketches, W, nw, dw, bitmap_out, sketch_out, s));
 }
 
+s2_status s2_encode_reduce_fused(const void* grad, s2_dtype dt, uint32_t W, uint64_t n, s2_params p,
+                                 uint32_t* bitmap_out, float* sketch_out, s2_stream_t stream) {
+    s2_status st = check_params(p);
+    if (st != S2_OK) return st;
+    if (dt != S2_F32 && dt != S2_BF16) return S2_ERR_INVALID_ARG;
+    if (n > kMaxN) return S2_ERR_UNSUPPORTED;
+    const uint64_t esz = dt == S2_F32 ? 4 : 2, nw = words_of(n), dw = (uint64_t)p.d * p.w;
+    const uint64_t gbytes = (uint64_t)W * n * esz;
+    if (!sketch_out || (nw > 0 && !bitmap_out) || (gbytes > 0 && !grad)) return S2_ERR_INVALID_ARG;
+    if (!aligned(grad, 16) || !aligned(bitmap_out, 16) || !aligned(sketch_out, 16)) return S2_ERR_ALIGNMENT;
+    if (overlap(grad, gbytes, bitmap_out, nw * 4) || overlap(grad, gbytes, sketch_out, dw * 4) ||
+        overlap(bitmap_out, nw * 4, sketch_out, dw * 4))
+        return S2_ERR_INVALID_ARG;
+    FusedArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.grad = grad;
+    a.bitmap = bitmap_out;
+    a.sketch = sketch_out;
+    a.n = n;
+    a.nw = nw;
+    a.workers = W;
+    a.d = p.d;
+    a.w = p.w;
+    a.keys = make_keys(p.seed, p.d);
+    return cuda_status(launch_fused(a, dt == S2_F32 ? 0 : 1, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 s2_status s2_decode_dense(const uint32_t* bitmap, const float* sketch, uint64_t n, s2_params p, float scale,
                           float* out, s2_stream_t stream) {
     s2_status st = check_decode_dense(bitmap, sketch, n, p, out);

@@ -44,6 +44,21 @@ cudaError_t launch_encode(const EncodeArgs& a, int dtype, bool vec, cudaStream_t
 cudaError_t launch_zero(float* p, uint64_t count, cudaStream_t s);
 cudaError_t take_encode_fault(unsigned int* out);
 
+// ---- fused encode + reduce (single sketch) ----------------------------------
+struct FusedArgs {
+    const void* grad;  // [W][n]
+    uint32_t* bitmap;  // [nw] aggregate (OR) bitmap
+    float* sketch;     // [d*w] summed sketch
+    uint64_t n;
+    uint64_t nw;
+    uint32_t workers;
+    uint32_t d;
+    uint32_t w;
+    RowKeys keys;
+};
+// Zero-fills the sketch, then one pass over all workers (dtype: 0 f32, 1 bf16).
+cudaError_t launch_fused(const FusedArgs& a, int dtype, cudaStream_t s);
+
 // ---- reduce ----------------------------------------------------------------
 cudaError_t launch_reduce(const uint32_t* bitmaps, const float* sketches, uint32_t W, uint64_t nw,
                           uint64_t dw, uint32_t* bitmap_out, float* sketch_out, cudaStream_t s);
