@@ -111,9 +111,9 @@ def measured_ceilings():
 
 def encode_launches(wl: workloads.Workload, l2_bytes: int) -> int:
     """Kernels one s2_encode_batched call launches: a zero fill and an encode per
-    group of workers whose sketches fit in 40% of L2 together."""
+    group of workers whose sketches fit in half of L2 together."""
     sk = 4 * wl.d * wl.w
-    group = max(1, min(wl.W, (l2_bytes * 2 // 5) // sk)) if sk else wl.W
+    group = max(1, min(wl.W, (l2_bytes // 2) // sk)) if sk else wl.W
     return 2 * ((wl.W + group - 1) // group)
 
 

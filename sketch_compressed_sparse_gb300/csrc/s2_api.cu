@@ -79,7 +79,7 @@ inline s2_status cuda_status(cudaError_t e) { return e == cudaSuccess ? S2_OK : 
 inline size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Encode W workers: zero the sketches and fill them, in groups of workers
-// whose sketches fit comfortably in L2 together, so that each group's
+// whose sketches fit in half of L2 together, so that each group's
 // sketches are zeroed, updated and written back once.
 s2_status encode_impl(const void* grad, s2_dtype dt, uint32_t W, uint64_t n, s2_params p, uint32_t* bitmaps,
                       float* sketches, cudaStream_t stream) {
@@ -90,7 +90,7 @@ s2_status encode_impl(const void* grad, s2_dtype dt, uint32_t W, uint64_t n, s2_
     cudaError_t e = device_info(&di);
     if (e != cudaSuccess) return S2_ERR_CUDA;
     const uint64_t sk_bytes = dw * 4;
-    uint64_t group = sk_bytes ? ((uint64_t)di.l2_bytes * 2 / 5) / sk_bytes : W;
+    uint64_t group = sk_bytes ? ((uint64_t)di.l2_bytes / 2) / sk_bytes : W;
     if (group < 1) group = 1;
     if (group > W) group = W;
     // vector loads need every worker row 16-byte aligned

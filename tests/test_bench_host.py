@@ -45,7 +45,7 @@ def test_select_workers_keeps_a_prefix():
 
 def test_encode_launch_groups():
     wl = workloads.Workload("e", 8, 1000, 5, 1 << 20, 0, "f32", [], [])  # 20 MiB sketch per worker
-    assert bench.encode_launches(wl, 126 << 20) == 2 * 4  # two workers per group
+    assert bench.encode_launches(wl, 126 << 20) == 2 * 3  # three workers per group
     wl = workloads.Workload("e", 4, 1000, 5, 1 << 22, 0, "f32", [], [])  # 80 MiB
     assert bench.encode_launches(wl, 126 << 20) == 2 * 4  # one worker per group
     wl = workloads.Workload("e", 8, 1000, 3, 1 << 19, 0, "f32", [], [])  # 6 MiB
