@@ -76,11 +76,34 @@ __device__ __forceinline__ void load_f32_task(uint4 (&v)[4], const float* g, uin
     }
 }
 
+// Nonzeros of sparse tasks wait in a per-warp list until 32 of them can be
+// inserted at once, one per lane (see encode_f32_vec).
+constexpr uint32_t kListCap = 64;
+constexpr uint32_t kDenseTask = 32;  // a task with at least this many nonzeros is walked per lane
+
+template <int D>
+__device__ __forceinline__ void insert_listed(const uint32_t* lpos, const float* lval, uint32_t cnt, int lane,
+                                              float* sk, int d, uint32_t w, const uint32_t* s_kh,
+                                              const uint32_t* s_ks, uint64_t keep) {
+    if ((uint32_t)lane < cnt) insert<D>(sk, lpos[lane], lval[lane], d, w, s_kh, s_ks, keep);
+}
+
+// fp32 rows, 16-byte aligned. Dense tasks (>= kDenseTask nonzeros, e.g. the
+// whole embedding rows) are inserted by each lane walking its own slots;
+// the nonzeros of sparse tasks (a few scattered values per 512 positions)
+// are appended to a per-warp list in shared memory instead, and inserted 32
+// at a time with every lane busy, so their d reductions do not run on lone
+// lanes. The list only holds one worker's entries; it is drained when the
+// warp moves on to another worker and at the end.
 template <int D>
 __global__ void __launch_bounds__(kThreads) encode_f32_vec(EncodeArgs a) {
     __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
+    __shared__ uint32_t s_lpos[kThreads / 32][kListCap];
+    __shared__ float s_lval[kThreads / 32][kListCap];
     load_keys(a.keys, s_kh, s_ks);
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t* lpos = s_lpos[warp];
+    float* lval = s_lval[warp];
     const uint64_t keep = policy_evict_last();
     const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
     uint32_t k = 0;
@@ -90,6 +113,7 @@ __global__ void __launch_bounds__(kThreads) encode_f32_vec(EncodeArgs a) {
         ++k;
     }
     const float* grad = reinterpret_cast<const float*>(a.grad);
+    uint32_t lcount = 0, lk = k;  // listed entries and their worker (warp-uniform)
     uint4 v[4];
     if (k < a.workers) load_f32_task(v, grad + (uint64_t)k * a.n, (uint64_t)local * kTaskElems, a.n, lane);
     for (; k < a.workers;) {
@@ -121,12 +145,49 @@ __global__ void __launch_bounds__(kThreads) encode_f32_vec(EncodeArgs a) {
             const uint64_t wi = (uint64_t)local * kTaskWords + lane;
             if (wi < a.nw) a.bitmaps[(uint64_t)k * a.nw + wi] = my_word;
         }
-        float* sk = a.sketches + (uint64_t)k * a.dw;
-        while (mask) {
-            const int slot = __ffs(mask) - 1;
-            mask &= mask - 1;
-            const uint32_t i = (uint32_t)(e0 + (slot >> 2) * 128 + lane * 4 + (slot & 3));
-            insert<D>(sk, i, __uint_as_float(pick16(v, slot)), a.d, a.w, s_kh, s_ks, keep);
+        uint32_t total;
+        const uint32_t excl = warp_exclusive_scan(__popc(mask), lane, &total);
+        if (total >= kDenseTask) {
+            float* sk = a.sketches + (uint64_t)k * a.dw;
+            while (mask) {
+                const int slot = __ffs(mask) - 1;
+                mask &= mask - 1;
+                const uint32_t i = (uint32_t)(e0 + (slot >> 2) * 128 + lane * 4 + (slot & 3));
+                insert<D>(sk, i, __uint_as_float(pick16(v, slot)), a.d, a.w, s_kh, s_ks, keep);
+            }
+        } else if (total > 0) {
+            if (k != lk && lcount > 0) {  // the list belongs to another worker: drain it first
+                insert_listed<D>(lpos, lval, lcount, lane, a.sketches + (uint64_t)lk * a.dw, a.d, a.w, s_kh, s_ks,
+                                 keep);
+                __syncwarp();
+                lcount = 0;
+            }
+            lk = k;
+            uint32_t at = lcount + excl;
+            for (uint32_t m = mask; m; m &= m - 1, ++at) {
+                const int slot = __ffs(m) - 1;
+                lpos[at] = (uint32_t)(e0 + (slot >> 2) * 128 + lane * 4 + (slot & 3));
+                lval[at] = __uint_as_float(pick16(v, slot));
+            }
+            lcount += total;  // at most 31 + 31 < kListCap
+            __syncwarp();
+            if (lcount >= 32) {
+                insert_listed<D>(lpos, lval, 32, lane, a.sketches + (uint64_t)lk * a.dw, a.d, a.w, s_kh, s_ks, keep);
+                const uint32_t rest = lcount - 32;
+                uint32_t p = 0;
+                float q = 0.f;
+                if ((uint32_t)lane < rest) {
+                    p = lpos[32 + lane];
+                    q = lval[32 + lane];
+                }
+                __syncwarp();
+                if ((uint32_t)lane < rest) {
+                    lpos[lane] = p;
+                    lval[lane] = q;
+                }
+                __syncwarp();
+                lcount = rest;
+            }
         }
         k = nk;
         local = nlocal;
@@ -137,6 +198,8 @@ __global__ void __launch_bounds__(kThreads) encode_f32_vec(EncodeArgs a) {
             load_f32_task(v, grad + (uint64_t)k * a.n, (uint64_t)local * kTaskElems, a.n, lane);
         }
     }
+    if (lcount > 0)
+        insert_listed<D>(lpos, lval, lcount, lane, a.sketches + (uint64_t)lk * a.dw, a.d, a.w, s_kh, s_ks, keep);
 }
 
 // ---- bf16, 16-byte vector loads --------------------------------------------
