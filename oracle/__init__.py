@@ -23,6 +23,9 @@ Parity status of each function (what pins it, in ``tests/test_oracle_pins.py``):
                      minority of colliding rows; brute force A A^T g at d = 1;
                      median equals numpy's median on planted sketches
   decode_compact     indices equal numpy's flatnonzero of the bitmap
+  encode_blocks /    block bitmap = numpy any() over each block; block size 1
+  decode_dense_blocks  equals the element functions; exact recovery of every
+                     position of marked blocks (zeros included) without collisions
 All functions are pinned; none is "parity unpinned".
 """
 from __future__ import annotations
@@ -82,6 +85,10 @@ def _load():
         lib.s2o_decode_dense.restype = None
         lib.s2o_decode_compact.argtypes = [vp, vp, vp, u64, u32, u32, u32, dbl, vp, vp, vp, u64]
         lib.s2o_decode_compact.restype = u64
+        lib.s2o_encode_blocks.argtypes = [vp, i32, u64, u64, u32, u32, u32, vp, vp, vp]
+        lib.s2o_encode_blocks.restype = None
+        lib.s2o_decode_dense_blocks.argtypes = [vp, vp, vp, u64, u64, u32, u32, u32, dbl, vp, vp]
+        lib.s2o_decode_dense_blocks.restype = None
         _lib = lib
         return lib
 
@@ -201,6 +208,49 @@ def decode_compact(bitmap: np.ndarray, S: np.ndarray, n: int, seed: int, scale: 
                                          _ptr(idx), _ptr(val), _ptr(amax), capacity))
     m = min(cnt, capacity)
     return cnt, idx[:m].copy(), val[:m].copy(), amax[:m].copy()
+
+
+def encode_blocks(grad: np.ndarray, block: int, d: int, w: int, seed: int, dtype: str = "f32"):
+    """Compression phase with one bitmap bit per block of `block` positions.
+
+    Returns (block bitmap uint32[ceil(nb/32)], S float64[d][w], A float64[d][w]).
+    """
+    g = np.ascontiguousarray(grad)
+    n = g.size
+    nb = (n + block - 1) // block
+    bm = np.empty(max(nwords(nb), 1), dtype=np.uint32)
+    S = np.empty((d, w), dtype=np.float64)
+    A = np.empty((d, w), dtype=np.float64)
+    _load().s2o_encode_blocks(_ptr(g), _DT[dtype], n, block, d, w, seed, _ptr(bm), _ptr(S), _ptr(A))
+    return bm[: nwords(nb)], S, A
+
+
+def decode_dense_blocks(bitmap: np.ndarray, S: np.ndarray, n: int, block: int, seed: int, scale: float = 1.0,
+                        A: Optional[np.ndarray] = None):
+    """Decompression with a block bitmap: every position of every marked block is queried."""
+    bitmap = np.ascontiguousarray(bitmap, dtype=np.uint32)
+    S = np.ascontiguousarray(S, dtype=np.float64)
+    d, w = S.shape
+    out = np.empty(n, dtype=np.float32)
+    amax = np.empty(n, dtype=np.float64)
+    Ap = None if A is None else np.ascontiguousarray(A, dtype=np.float64)
+    _load().s2o_decode_dense_blocks(_ptr(bitmap), _ptr(S), _ptr(Ap), n, block, d, w, seed, float(scale), _ptr(out),
+                                    _ptr(amax))
+    return out, amax
+
+
+def pipeline_blocks(grad: np.ndarray, block: int, d: int, w: int, seed: int, dtype: str = "f32", scale: float = 1.0):
+    """Every worker compresses with a block bitmap; aggregate; decode every marked block."""
+    W, n = grad.shape
+    nb = (n + block - 1) // block
+    bms = np.zeros((W, nwords(nb)), dtype=np.uint32)
+    S = np.empty((W, d, w), dtype=np.float64)
+    A = np.empty((W, d, w), dtype=np.float64)
+    for k in range(W):
+        bms[k], S[k], A[k] = encode_blocks(grad[k], block, d, w, seed, dtype)
+    bm, Ssum, Asum = reduce(bms, S, A)
+    out, amax = decode_dense_blocks(bm, Ssum, n, block, seed, scale, Asum)
+    return dict(bitmaps=bms, S=S, A=A, bitmap=bm, S_sum=Ssum, A_sum=Asum, out=out, amax=amax)
 
 
 def encode_all(grad: np.ndarray, d: int, w: int, seed: int, dtype: str = "f32"):

@@ -291,3 +291,50 @@ uint64_t s2o_decode_compact(const uint32_t *bitmap, const double *S, const doubl
     }
     return t;
 }
+
+/* ---- block-granular bitmap ----------------------------------------------- */
+
+/*
+ * Section 3.1 "Compressing Sparse Gradient" in the paper's own granularity:
+ * one bitmap bit per block of `block` consecutive positions (an embedding
+ * row, a gradient block); block x is marked iff it holds a nonzero. The
+ * sketch is the same as s2o_encode's: only nonzero positions are inserted.
+ * bitmap: ceil(ceil(n/block)/32) words.
+ */
+void s2o_encode_blocks(const void *grad, int dt, uint64_t n, uint64_t block, uint32_t d, uint32_t w,
+                       uint32_t seed, uint32_t *bitmap, double *S, double *A)
+{
+    uint64_t nb = (n + block - 1) / block;
+    uint64_t nw = (n + 31) / 32;
+    uint32_t *elem = (uint32_t *)calloc(nw ? nw : 1, sizeof(uint32_t));
+    s2o_encode(grad, dt, n, d, w, seed, elem, S, A);
+    memset(bitmap, 0, ((nb + 31) / 32) * sizeof(uint32_t));
+    for (uint64_t x = 0; x < n; ++x)
+        if (bit_is_set(elem, x))
+            bitmap[(x / block) >> 5] |= 1u << ((x / block) & 31);
+    free(elem);
+}
+
+/*
+ * Decompression with a block bitmap: Sparse(g) is every position of every
+ * marked block (zeros inside a marked block included); each is queried as in
+ * s2o_decode_dense, every other position gets +0.0f.
+ */
+void s2o_decode_dense_blocks(const uint32_t *bitmap, const double *S, const double *A, uint64_t n,
+                             uint64_t block, uint32_t d, uint32_t w, uint32_t seed, double scale,
+                             float *out, double *amax)
+{
+    for (uint64_t i = 0; i < n; ++i) {
+        if (!bit_is_set(bitmap, i / block)) {
+            out[i] = 0.0f;
+            if (amax)
+                amax[i] = 0.0;
+            continue;
+        }
+        double am;
+        double med = query(S, A, (uint32_t)i, d, w, seed, &am);
+        out[i] = (float)(scale * med);
+        if (amax)
+            amax[i] = am;
+    }
+}

@@ -392,3 +392,47 @@ def test_tiny_workload_pipeline_invariants():
     # estimates are finite and bounded by the largest bucket magnitude
     assert np.isfinite(res["out"]).all()
     assert (np.abs(res["out"][union]) <= res["amax"][union] + 1e-6).all()
+
+
+# ----------------------------------------------------------------- block-granular bitmap
+
+@pytest.mark.parametrize("block", [1, 7, 32, 512])
+def test_block_bitmap_marks_blocks_with_a_nonzero(block):
+    # Section 3.1: one bit per block, set iff the block holds a nonzero
+    n = 5000
+    rng = np.random.default_rng(block)
+    g = np.zeros(n, dtype=np.float32)
+    pos = rng.choice(n, size=40, replace=False)
+    g[pos] = rng.normal(size=40).astype(np.float32)
+    g[rng.choice(n, size=10)] = np.float32(-0.0)
+    bm, S, _ = oracle.encode_blocks(g, block, 3, 64, 5)
+    nb = (n + block - 1) // block
+    padded = np.zeros(nb * block, dtype=bool)
+    padded[:n] = g.view(np.uint32) & 0x7FFFFFFF != 0
+    np.testing.assert_array_equal(bm, support_bitmap(padded.reshape(nb, block).any(axis=1)))
+    _, S_elem, _ = oracle.encode(g, 3, 64, 5)
+    np.testing.assert_array_equal(S, S_elem)  # zeros are never inserted: same sketch
+
+
+def test_block_size_one_is_the_element_path():
+    wl = workloads.custom(W=3, n=3000, d=5, w=97, density=0.05, tag=81)
+    G = wl.dense()
+    rb = oracle.pipeline_blocks(G, 1, wl.d, wl.w, wl.seed)
+    re_ = oracle.pipeline(G, wl.d, wl.w, wl.seed)
+    np.testing.assert_array_equal(rb["bitmap"], re_["bitmap"])
+    np.testing.assert_array_equal(rb["out"], re_["out"])
+
+
+def test_block_decode_recovers_whole_blocks_exactly_without_collisions():
+    # every position of a marked block is recovered, the zeros in it as 0.0
+    n, block, d, w, seed = 8192, 512, 3, 1 << 22, 9
+    G = np.zeros((2, n), dtype=np.float32)
+    G[0, 512:560] = np.arange(1, 49, dtype=np.float32)
+    G[1, 4096 + 100] = -7.0
+    res = oracle.pipeline_blocks(G, block, d, w, seed)
+    marked = np.zeros(n, dtype=bool)
+    marked[512:1024] = True
+    marked[4096:4608] = True
+    np.testing.assert_array_equal(unpack_bits(res["bitmap"], n // block), [False, True] + [False] * 6 + [True] + [False] * 6 + [False])
+    assert (res["out"][~marked] == 0).all()
+    np.testing.assert_array_equal(res["out"][marked], G.sum(axis=0)[marked])
