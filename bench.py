@@ -44,7 +44,13 @@ FLUSH_BYTES = 512 << 20
 
 # ---------------------------------------------------------------- byte accounting
 
-def algorithmic_bytes(wl: workloads.Workload, nnz_union: int) -> dict:
+def bitmap_bytes(n: int, block: int = 0) -> int:
+    """Bytes of one bitmap: one bit per position, or per block of `block` positions."""
+    bits = n if not block else (n + block - 1) // block
+    return 4 * ((bits + 31) // 32)
+
+
+def algorithmic_bytes(wl: workloads.Workload, nnz_union: int, block: int = 0) -> dict:
     """Bytes each stage must move at minimum (each structure read/written once).
 
     encode: read grad, write W bitmaps and W sketches;
@@ -54,7 +60,7 @@ def algorithmic_bytes(wl: workloads.Workload, nnz_union: int) -> dict:
     """
     W, n, d, w = wl.W, wl.n, wl.d, wl.w
     E = wl.elem_bytes
-    BM = 4 * ((n + 31) // 32)
+    BM = bitmap_bytes(n, block)
     SK = 4 * d * w
     enc = W * n * E + W * BM + W * SK
     red = W * (SK + BM) + SK + BM
@@ -79,7 +85,7 @@ def l2_sector_ops_fused(wl: workloads.Workload, nnz_union: int) -> dict:
     return {"encode_reduce_fused": fused, "decode": ops["decode"], "total": fused + ops["decode"]}
 
 
-def l2_sector_ops(wl: workloads.Workload, nnz_union: int) -> dict:
+def l2_sector_ops(wl: workloads.Workload, nnz_union: int, block: int = 0) -> dict:
     """32-byte L2 sector operations each stage issues at minimum.
 
     Streams count one operation per 32-byte sector; every scattered 4-byte
@@ -91,7 +97,7 @@ def l2_sector_ops(wl: workloads.Workload, nnz_union: int) -> dict:
     """
     W, n, d, w = wl.W, wl.n, wl.d, wl.w
     sec = lambda b: (b + 31) // 32
-    BM = 4 * ((n + 31) // 32)
+    BM = bitmap_bytes(n, block)
     SK = 4 * d * w
     nnz = sum(wl.nnz_per_worker)
     enc = sec(W * n * wl.elem_bytes) + W * sec(BM) + W * sec(SK) + nnz * d
@@ -263,11 +269,14 @@ def run_ours(args, wl, world, rank, local):
     W, n, d, w, seed = wl.W, wl.n, wl.d, wl.w, wl.seed
     nnz_u = wl.union_nnz()
     grad = wl.dense_torch(dev)
+    blk = args.block
+    nbits = (n + blk - 1) // blk if blk else n  # bits of one bitmap
     if args.mode == "fused":
         bitmaps = sketches = None
     else:
-        bitmaps, sketches = s2.alloc_encode_outputs(W, n, d, w, dev)
-    bitmap = torch.empty(s2.nwords(n), dtype=torch.int32, device=dev)
+        bitmaps = torch.empty((W, s2.nwords(nbits)), dtype=torch.int32, device=dev)
+        sketches = torch.empty((W, d, w), dtype=torch.float32, device=dev)
+    bitmap = torch.empty(s2.nwords(nbits), dtype=torch.int32, device=dev)
     sketch = torch.empty((d, w), dtype=torch.float32, device=dev)
     out = torch.empty(n, dtype=torch.float32, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -275,13 +284,25 @@ def run_ours(args, wl, world, rank, local):
 
     fused = args.mode == "fused"
 
+    def encode():
+        if blk:
+            s2.s2_encode_batched_blocks(grad, blk, d, w, seed, bitmaps, sketches)
+        else:
+            s2.s2_encode_batched(grad, d, w, seed, bitmaps, sketches)
+
+    def decode():
+        if blk:
+            s2.s2_decode_dense_blocks(bitmap, sketch, n, blk, d, w, seed, out)
+        else:
+            s2.s2_decode_dense(bitmap, sketch, n, d, w, seed, out)
+
     def step():
         if fused:
             s2.s2_encode_reduce_fused(grad, d, w, seed, bitmap, sketch)
         else:
-            s2.s2_encode_batched(grad, d, w, seed, bitmaps, sketches)
-            s2.s2_reduce(bitmaps, sketches, n, d, w, bitmap, sketch)
-        s2.s2_decode_dense(bitmap, sketch, n, d, w, seed, out)
+            encode()
+            s2.s2_reduce(bitmaps, sketches, nbits, d, w, bitmap, sketch)
+        decode()
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
@@ -305,11 +326,11 @@ def run_ours(args, wl, world, rank, local):
                 s2.s2_encode_reduce_fused(grad, d, w, seed, bitmap, sketch)
                 e[1].record(stream)
             else:
-                s2.s2_encode_batched(grad, d, w, seed, bitmaps, sketches)
+                encode()
                 e[1].record(stream)
-                s2.s2_reduce(bitmaps, sketches, n, d, w, bitmap, sketch)
+                s2.s2_reduce(bitmaps, sketches, nbits, d, w, bitmap, sketch)
             e[2].record(stream)
-            s2.s2_decode_dense(bitmap, sketch, n, d, w, seed, out)
+            decode()
             e[3].record(stream)
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - wall0
@@ -324,7 +345,7 @@ def run_ours(args, wl, world, rank, local):
     elapsed, units = combine_over_ranks(total_ms / 1e3, float(W * n * K), world, dev)
     value = units / elapsed / 1e9
 
-    by = algorithmic_bytes(wl, nnz_u)
+    by = algorithmic_bytes(wl, nnz_u, blk)
     peaks = measured_peaks()
     peak = peaks["hbm_gbs"]
     enc_s = enc_ms / 1e3 / K
@@ -362,7 +383,7 @@ def run_ours(args, wl, world, rank, local):
         "gpu_launches": K * (n_enc + 2),
         "wall_ms_timed_region": round(wall * 1e3, 3),
     }
-    ops = l2_sector_ops(wl, nnz_u)
+    ops = l2_sector_ops(wl, nnz_u, blk)
     ceil = measured_ceilings()
     step_s = total_ms / 1e3 / K
     l2 = {"unit": "G sector ops/s", "ops_per_step": ops, "achieved": round(ops["total"] / step_s / 1e9, 1)}
@@ -372,6 +393,9 @@ def run_ours(args, wl, world, rank, local):
                   peak_source="scattered red.f32 rate measured by bench.py --ceilings (profiles/ceilings_gb300.json)")
     res["l2_roofline"] = l2
     res["config"]["mode"] = "per_worker (encode_batched + reduce + decode_dense)"
+    if blk:
+        res["config"]["mode"] = f"per_worker, block bitmap of {blk} positions (encode_batched_blocks + reduce + decode_dense_blocks)"
+        res["gpu_launches"] = K * (n_enc + 1 + 2)  # + the block bitmaps' zero fill
     if fused:
         # same step with encode + reduce replaced by the fused single-sketch pass
         byf = algorithmic_bytes_fused(wl, nnz_u)
@@ -505,6 +529,8 @@ def main(argv=None):
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
     ap.add_argument("--mode", choices=["per_worker", "fused"], default="per_worker",
                     help="per_worker: the simulated data-parallel path (default); fused: encode_reduce_fused + decode")
+    ap.add_argument("--block", type=int, default=0,
+                    help="positions per bitmap bit (a multiple of 32; 0 = one bit per position, the default)")
     ap.add_argument("--workers", type=int, default=None,
                     help="profiling aid: keep only the first K workers of the workload (changes the workload)")
     ap.add_argument("--ceilings", action="store_true",

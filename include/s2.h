@@ -107,6 +107,22 @@ S2_API s2_status s2_encode_batched(const void *grad, s2_dtype dt, uint32_t W, ui
                             uint32_t *bitmaps, float *sketches, s2_stream_t stream);
 
 /*
+ * s2_encode_batched_blocks -- s2_encode_batched with the paper's block-granular
+ * bitmap (Section 3.1 "Compressing Sparse Gradient": one bit per word vector
+ * or gradient block, set iff the block contains a nonzero).
+ *   block: positions per block, a multiple of 32 (S2_ERR_UNSUPPORTED
+ *   otherwise); nb = ceil(n / block) blocks, nbw = ceil(nb / 32) words.
+ *   block_bitmaps [W][nbw] uint32 out: bit x of worker k set iff positions
+ *   [x*block, (x+1)*block) of worker k hold a nonzero (same bit layout as the
+ *   element bitmap, over blocks).
+ *   sketches: exactly as s2_encode_batched (only nonzero positions are
+ *   inserted). Aggregate the block bitmaps with s2_reduce passing nb as n.
+ */
+S2_API s2_status s2_encode_batched_blocks(const void *grad, s2_dtype dt, uint32_t W, uint64_t n, uint32_t block,
+                                          s2_params p, uint32_t *block_bitmaps, float *sketches,
+                                          s2_stream_t stream);
+
+/*
  * s2_reduce -- the AllReduce(S, C) of Algorithm 1 (Section 3.1 "Collecting
  * Sparse-Sketch with AllReduce"), with all W workers resident on this GPU.
  *   bitmaps [W][nw], sketches [W][d][w]  in.
@@ -146,6 +162,18 @@ S2_API s2_status s2_encode_reduce_fused(const void *grad, s2_dtype dt, uint32_t 
  */
 S2_API s2_status s2_decode_dense(const uint32_t *bitmap, const float *sketch, uint64_t n, s2_params p,
                           float scale, float *out, s2_stream_t stream);
+
+/*
+ * s2_decode_dense_blocks -- s2_decode_dense under a block bitmap (Section 3.1
+ * "Decompressing Sparse Gradient": the recovered indices are every position
+ * of every marked block, zeros inside a marked block included).
+ *   block_bitmap [nbw] (from s2_reduce over block bitmaps), block as in
+ *   s2_encode_batched_blocks; out [n]: the median estimate at every position
+ *   of a marked block, +0.0f elsewhere.
+ */
+S2_API s2_status s2_decode_dense_blocks(const uint32_t *block_bitmap, const float *sketch, uint64_t n,
+                                        uint32_t block, s2_params p, float scale, float *out,
+                                        s2_stream_t stream);
 
 /* Device workspace bytes that s2_decode_compact needs for length n. */
 S2_API s2_status s2_decode_workspace_size(uint64_t n, size_t *bytes);

@@ -26,6 +26,8 @@ __all__ = [
     "s2_encode_batched",
     "s2_reduce",
     "s2_encode_reduce_fused",
+    "s2_encode_batched_blocks",
+    "s2_decode_dense_blocks",
     "s2_decode_dense",
     "s2_decode_workspace_size",
     "s2_decode_compact",
@@ -59,6 +61,8 @@ _SIGS = {
     "s2_encode_batched": ([_vp, _i32, _u32, _u64, Params, _vp, _vp, _vp], _i32),
     "s2_reduce": ([_vp, _vp, _u32, _u64, Params, _vp, _vp, _vp], _i32),
     "s2_encode_reduce_fused": ([_vp, _i32, _u32, _u64, Params, _vp, _vp, _vp], _i32),
+    "s2_encode_batched_blocks": ([_vp, _i32, _u32, _u64, _u32, Params, _vp, _vp, _vp], _i32),
+    "s2_decode_dense_blocks": ([_vp, _vp, _u64, _u32, Params, _f32, _vp, _vp], _i32),
     "s2_decode_dense": ([_vp, _vp, _u64, Params, _f32, _vp, _vp], _i32),
     "s2_decode_workspace_size": ([_u64, ctypes.POINTER(_sz)], _i32),
     "s2_decode_compact": ([_vp, _vp, _u64, Params, _f32, _vp, _vp, _u64, _vp, _vp, _sz, _vp], _i32),
@@ -197,6 +201,32 @@ def s2_encode_reduce_fused(grad: torch.Tensor, d: int, w: int, seed: int, bitmap
                                         _dev(bitmap_out, "bitmap_out", _U32, nwords(n)),
                                         _dev(sketch_out, "sketch_out", (torch.float32,), d * w), _stream(stream)),
            "s2_encode_reduce_fused")
+
+
+def nblockwords(n: int, block: int) -> int:
+    return nwords((n + block - 1) // block)
+
+
+def s2_encode_batched_blocks(grad: torch.Tensor, block: int, d: int, w: int, seed: int, block_bitmaps: torch.Tensor,
+                             sketches: torch.Tensor, stream=None) -> None:
+    """W workers, one bitmap bit per block: grad [W, n] -> block_bitmaps [W, nbw], sketches [W, d, w]."""
+    if grad.dim() != 2:
+        raise ValueError("grad must be [W, n]")
+    W, n = grad.shape
+    _check(_f("s2_encode_batched_blocks")(_dev(grad, "grad", _GRAD), _dtype_code(grad), W, n, block,
+                                          Params(d, w, seed),
+                                          _dev(block_bitmaps, "block_bitmaps", _U32, W * nblockwords(n, block)),
+                                          _dev(sketches, "sketches", (torch.float32,), W * d * w), _stream(stream)),
+           "s2_encode_batched_blocks")
+
+
+def s2_decode_dense_blocks(block_bitmap: torch.Tensor, sketch: torch.Tensor, n: int, block: int, d: int, w: int,
+                           seed: int, out: torch.Tensor, scale: float = 1.0, stream=None) -> None:
+    """Decode every position of every marked block: block_bitmap [nbw], sketch [d, w] -> out [n]."""
+    _check(_f("s2_decode_dense_blocks")(_dev(block_bitmap, "block_bitmap", _U32, nblockwords(n, block)),
+                                        _dev(sketch, "sketch", (torch.float32,), d * w), n, block,
+                                        Params(d, w, seed), scale, _dev(out, "out", (torch.float32,), n),
+                                        _stream(stream)), "s2_decode_dense_blocks")
 
 
 def s2_decode_dense(bitmap: torch.Tensor, sketch: torch.Tensor, n: int, d: int, w: int, seed: int,

@@ -82,7 +82,7 @@ inline size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 // whose sketches fit in half of L2 together, so that each group's
 // sketches are zeroed, updated and written back once.
 s2_status encode_impl(const void* grad, s2_dtype dt, uint32_t W, uint64_t n, s2_params p, uint32_t* bitmaps,
-                      float* sketches, cudaStream_t stream) {
+                      float* sketches, cudaStream_t stream, uint32_t block = 0) {
     const uint64_t esz = dt == S2_F32 ? 4 : 2;
     const uint64_t nw = words_of(n);
     const uint64_t dw = (uint64_t)p.d * p.w;
@@ -104,12 +104,19 @@ s2_status encode_impl(const void* grad, s2_dtype dt, uint32_t W, uint64_t n, s2_
     a.d = p.d;
     a.w = p.w;
     a.keys = make_keys(p.seed, p.d);
+    const uint64_t nbw = block ? words_of((n + block - 1) / block) : 0;
+    a.block_words = block / 32;
+    a.nbw = nbw;
+    if (block && W * nbw) {  // block bits are set with atomicOr: start from zero
+        e = launch_zero(reinterpret_cast<float*>(bitmaps), W * nbw, stream);
+        if (e != cudaSuccess) return S2_ERR_CUDA;
+    }
     for (uint64_t k0 = 0; k0 < W; k0 += group) {
         const uint64_t g = (W - k0) < group ? (W - k0) : group;
         e = launch_zero(sketches + k0 * dw, g * dw, stream);
         if (e != cudaSuccess) return S2_ERR_CUDA;
         a.grad = static_cast<const char*>(grad) + k0 * n * esz;
-        a.bitmaps = bitmaps + k0 * nw;
+        a.bitmaps = bitmaps + k0 * (block ? nbw : nw);
         a.sketches = sketches + k0 * dw;
         a.workers = (uint32_t)g;
         e = launch_encode(a, dt == S2_F32 ? 0 : 1, vec, stream);
@@ -221,6 +228,42 @@ s2_status s2_encode_batched(const void* grad, s2_dtype dt, uint32_t W, uint64_t 
     s2_status st = check_encode(grad, dt, W, n, p, bitmaps, sketches);
     if (st != S2_OK || W == 0) return st;
     return encode_impl(grad, dt, W, n, p, bitmaps, sketches, reinterpret_cast<cudaStream_t>(stream));
+}
+
+s2_status s2_encode_batched_blocks(const void* grad, s2_dtype dt, uint32_t W, uint64_t n, uint32_t block,
+                                   s2_params p, uint32_t* block_bitmaps, float* sketches, s2_stream_t stream) {
+    s2_status st = check_params(p);
+    if (st != S2_OK) return st;
+    if (dt != S2_F32 && dt != S2_BF16) return S2_ERR_INVALID_ARG;
+    if (block == 0 || block % 32 != 0) return S2_ERR_UNSUPPORTED;
+    if (n > kMaxN) return S2_ERR_UNSUPPORTED;
+    if (W == 0) return S2_OK;
+    const uint64_t esz = dt == S2_F32 ? 4 : 2;
+    const uint64_t nbw = words_of((n + block - 1) / block);
+    const uint64_t gbytes = (uint64_t)W * n * esz, bbytes = (uint64_t)W * nbw * 4,
+                   sbytes = (uint64_t)W * p.d * p.w * 4;
+    if (!sketches || (n > 0 && (!grad || !block_bitmaps))) return S2_ERR_INVALID_ARG;
+    if (!aligned(grad, 16) || !aligned(block_bitmaps, 16) || !aligned(sketches, 16)) return S2_ERR_ALIGNMENT;
+    if (overlap(grad, gbytes, block_bitmaps, bbytes) || overlap(grad, gbytes, sketches, sbytes) ||
+        overlap(block_bitmaps, bbytes, sketches, sbytes))
+        return S2_ERR_INVALID_ARG;
+    return encode_impl(grad, dt, W, n, p, block_bitmaps, sketches, reinterpret_cast<cudaStream_t>(stream), block);
+}
+
+s2_status s2_decode_dense_blocks(const uint32_t* block_bitmap, const float* sketch, uint64_t n, uint32_t block,
+                                 s2_params p, float scale, float* out, s2_stream_t stream) {
+    s2_status st = check_params(p);
+    if (st != S2_OK) return st;
+    if (block == 0 || block % 32 != 0 || n > kMaxN) return S2_ERR_UNSUPPORTED;
+    if (n == 0) return S2_OK;
+    if (!block_bitmap || !sketch || !out) return S2_ERR_INVALID_ARG;
+    if (!aligned(block_bitmap, 16) || !aligned(sketch, 16) || !aligned(out, 16)) return S2_ERR_ALIGNMENT;
+    const uint64_t dw = (uint64_t)p.d * p.w, nbw = words_of((n + block - 1) / block);
+    if (overlap(out, n * 4, block_bitmap, nbw * 4) || overlap(out, n * 4, sketch, dw * 4)) return S2_ERR_INVALID_ARG;
+    DecodeArgs a = make_decode_args(block_bitmap, sketch, n, p, scale);
+    a.nw = nbw;
+    a.block = block;
+    return cuda_status(launch_decode_dense(a, out, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 s2_status s2_reduce(const uint32_t* bitmaps, const float* sketches, uint32_t W, uint64_t n, s2_params p,

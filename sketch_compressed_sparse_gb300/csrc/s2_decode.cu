@@ -82,7 +82,26 @@ __device__ __forceinline__ void gather_hint(float (&e)[(D > 0 ? D : kMaxRows)], 
 // 16-byte streaming stores, +0.0f at unset positions.
 constexpr int kPop = 2;
 
-template <int D>
+// This lane's 16 slots of a task under a block bitmap: position p is set iff
+// block p / a.block is marked. A lane's 4 consecutive positions never
+// straddle a block (blocks are multiples of 32 positions).
+__device__ __forceinline__ uint32_t lane_mask_blocks(const DecodeArgs& a, uint64_t e0, int lane) {
+    uint32_t mask = 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const uint64_t p = e0 + u * 128 + lane * 4;
+        if (p < a.n) {
+            const uint32_t blk = (uint32_t)p / a.block;  // positions are below 2^32
+            if ((__ldg(a.bitmap + (blk >> 5)) >> (blk & 31)) & 1u) {
+                const uint64_t left = a.n - p;
+                mask |= (left >= 4 ? 0xfu : ((1u << left) - 1u)) << (4 * u);
+            }
+        }
+    }
+    return mask;
+}
+
+template <int D, bool BLK>
 __global__ void __launch_bounds__(kThreads) decode_dense_kernel(DecodeArgs a, float* __restrict__ out) {
     __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
     load_keys(a.keys, s_kh, s_ks);
@@ -93,8 +112,13 @@ __global__ void __launch_bounds__(kThreads) decode_dense_kernel(DecodeArgs a, fl
     for (uint64_t t = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < ntasks; t += nwarps) {
         const uint64_t e0 = t * kTaskElems;
         const uint64_t wi = t * kTaskWords + lane;
-        const uint32_t my_word = lane < kTaskWords ? load_word(a.bitmap, wi, a.nw, a.n) : 0u;
-        uint32_t mask = lane_mask(my_word, lane);
+        uint32_t mask;
+        if (BLK) {
+            mask = lane_mask_blocks(a, e0, lane);
+        } else {
+            const uint32_t my_word = lane < kTaskWords ? load_word(a.bitmap, wi, a.nw, a.n) : 0u;
+            mask = lane_mask(my_word, lane);
+        }
         float r[16];
 #pragma unroll
         for (int s = 0; s < 16; ++s) r[s] = 0.f;
@@ -270,12 +294,17 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-template <int D>
-cudaError_t launch_dense_d(const DecodeArgs& a, float* out, cudaStream_t s) {
+template <int D, bool BLK>
+cudaError_t launch_dense_db(const DecodeArgs& a, float* out, cudaStream_t s) {
     const uint64_t tasks = (a.n + kTaskElems - 1) / kTaskElems;
     const uint64_t blocks = (tasks + (kThreads / 32) - 1) / (kThreads / 32);
-    decode_dense_kernel<D><<<grid_for(decode_dense_kernel<D>, blocks), kThreads, 0, s>>>(a, out);
+    decode_dense_kernel<D, BLK><<<grid_for(decode_dense_kernel<D, BLK>, blocks), kThreads, 0, s>>>(a, out);
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_dense_d(const DecodeArgs& a, float* out, cudaStream_t s) {
+    return a.block ? launch_dense_db<D, true>(a, out, s) : launch_dense_db<D, false>(a, out, s);
 }
 
 template <int D>

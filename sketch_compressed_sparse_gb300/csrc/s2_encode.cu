@@ -56,6 +56,25 @@ __device__ __forceinline__ void load_keys(const RowKeys& k, uint32_t* s_kh, uint
     __syncthreads();
 }
 
+// Store word wi of worker k's bitmap (lanes with valid = true hold one). With
+// BLK, the bitmap is a block bitmap (one bit per a.block_words words, zeroed
+// beforehand): every block that holds a nonzero word is marked once per task
+// with an atomicOr; lanes marking the same block are merged first. Called by
+// all 32 lanes.
+template <bool BLK>
+__device__ __forceinline__ void store_bitmap_word(const EncodeArgs& a, uint32_t k, uint64_t wi, uint32_t word,
+                                                  bool valid, int lane) {
+    if (!BLK) {
+        if (valid) a.bitmaps[(uint64_t)k * a.nw + wi] = word;
+    } else {
+        const bool mark = valid && word != 0;
+        const unsigned long long blk = mark ? wi / a.block_words : ~0ull;
+        const unsigned grp = __match_any_sync(kFull, blk);
+        if (mark && __ffs(grp) - 1 == lane)
+            atomicOr(a.bitmaps + (uint64_t)k * a.nbw + (blk >> 5), 1u << (blk & 31));
+    }
+}
+
 // ---- fp32, 16-byte vector loads --------------------------------------------
 // Lane l loads positions u*128 + 4l .. +3 of the task for u = 0..3; slot
 // 4u + c is position u*128 + 4l + c. Word q of chunk u is made of the
@@ -95,7 +114,7 @@ __device__ __forceinline__ void insert_listed(const uint32_t* lpos, const float*
 // at a time with every lane busy, so their d reductions do not run on lone
 // lanes. The list only holds one worker's entries; it is drained when the
 // warp moves on to another worker and at the end.
-template <int D>
+template <int D, bool BLK>
 __global__ void __launch_bounds__(kThreads) encode_f32_vec(EncodeArgs a) {
     __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
     __shared__ uint32_t s_lpos[kThreads / 32][kListCap];
@@ -141,9 +160,9 @@ __global__ void __launch_bounds__(kThreads) encode_f32_vec(EncodeArgs a) {
             uint32_t got = __shfl_sync(kFull, part, (lane & 3) * 8);
             if ((lane >> 2) == u) my_word = got;
         }
-        if (lane < kTaskWords) {
+        {
             const uint64_t wi = (uint64_t)local * kTaskWords + lane;
-            if (wi < a.nw) a.bitmaps[(uint64_t)k * a.nw + wi] = my_word;
+            store_bitmap_word<BLK>(a, k, wi, my_word, lane < kTaskWords && wi < a.nw, lane);
         }
         uint32_t total;
         const uint32_t excl = warp_exclusive_scan(__popc(mask), lane, &total);
@@ -206,7 +225,7 @@ __global__ void __launch_bounds__(kThreads) encode_f32_vec(EncodeArgs a) {
 // Lane l loads positions u*256 + 8l .. +7 for u = 0..1; slot 8u + c is
 // position u*256 + 8l + c. Word q of chunk u is made of the bytes of lanes
 // 4q .. 4q+3.
-template <int D>
+template <int D, bool BLK>
 __global__ void __launch_bounds__(kThreads) encode_bf16_vec(EncodeArgs a) {
     __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
     load_keys(a.keys, s_kh, s_ks);
@@ -254,9 +273,9 @@ __global__ void __launch_bounds__(kThreads) encode_bf16_vec(EncodeArgs a) {
             uint32_t got = __shfl_sync(kFull, part, (lane & 7) * 4);
             if ((lane >> 3) == u) my_word = got;
         }
-        if (lane < kTaskWords) {
+        {
             const uint64_t wi = (uint64_t)local * kTaskWords + lane;
-            if (wi < a.nw) a.bitmaps[(uint64_t)k * a.nw + wi] = my_word;
+            store_bitmap_word<BLK>(a, k, wi, my_word, lane < kTaskWords && wi < a.nw, lane);
         }
         float* sk = a.sketches + (uint64_t)k * a.dw;
         while (mask) {
@@ -280,7 +299,7 @@ __global__ void __launch_bounds__(kThreads) encode_bf16_vec(EncodeArgs a) {
 // ---- any alignment: one element per lane and load -------------------------
 // Lane l loads position u*32 + l for u = 0..15; a ballot gives word u
 // directly; slot u is position u*32 + l.
-template <int D, bool BF16>
+template <int D, bool BF16, bool BLK>
 __global__ void __launch_bounds__(kThreads) encode_scalar(EncodeArgs a) {
     __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
     load_keys(a.keys, s_kh, s_ks);
@@ -318,9 +337,9 @@ __global__ void __launch_bounds__(kThreads) encode_scalar(EncodeArgs a) {
             mask |= (uint32_t)nz << u;
             if (lane == u) my_word = word;
         }
-        if (lane < kTaskWords) {
+        {
             const uint64_t wi = (uint64_t)local * kTaskWords + lane;
-            if (wi < a.nw) a.bitmaps[(uint64_t)k * a.nw + wi] = my_word;
+            store_bitmap_word<BLK>(a, k, wi, my_word, lane < kTaskWords && wi < a.nw, lane);
         }
         float* sk = a.sketches + (uint64_t)k * a.dw;
         while (mask) {
@@ -559,28 +578,33 @@ cudaError_t launch_bulk(const EncodeArgs& a, uint64_t tasks, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <int D>
-cudaError_t launch_encode_d(const EncodeArgs& a, int dtype, bool vec, cudaStream_t s) {
+template <int D, bool BLK>
+cudaError_t launch_encode_db(const EncodeArgs& a, int dtype, bool vec, cudaStream_t s) {
     const uint64_t tasks = (uint64_t)a.workers * a.tasks_per_worker;
     const uint64_t blocks = (tasks + (kThreads / 32) - 1) / (kThreads / 32);
     const uint64_t esz = dtype == 0 ? 4 : 2;
     const bool rows_aligned = (a.n * esz) % 16 == 0;
-    if (kUseBulk && vec && rows_aligned) {
+    if (!BLK && kUseBulk && vec && rows_aligned) {
         EncodeArgs b = a;  // bulk tasks are 2 KB of gradient
         b.tasks_per_worker = (uint32_t)((a.n * esz + kBulkTaskBytes - 1) / kBulkTaskBytes);
         const uint64_t btasks = (uint64_t)b.workers * b.tasks_per_worker;
         return dtype == 0 ? launch_bulk<D, false>(b, btasks, s) : launch_bulk<D, true>(b, btasks, s);
     }
     if (vec && dtype == 0) {
-        encode_f32_vec<D><<<grid_for(encode_f32_vec<D>, blocks), kThreads, 0, s>>>(a);
+        encode_f32_vec<D, BLK><<<grid_for(encode_f32_vec<D, BLK>, blocks), kThreads, 0, s>>>(a);
     } else if (vec && dtype == 1) {
-        encode_bf16_vec<D><<<grid_for(encode_bf16_vec<D>, blocks), kThreads, 0, s>>>(a);
+        encode_bf16_vec<D, BLK><<<grid_for(encode_bf16_vec<D, BLK>, blocks), kThreads, 0, s>>>(a);
     } else if (dtype == 0) {
-        encode_scalar<D, false><<<grid_for(encode_scalar<D, false>, blocks), kThreads, 0, s>>>(a);
+        encode_scalar<D, false, BLK><<<grid_for(encode_scalar<D, false, BLK>, blocks), kThreads, 0, s>>>(a);
     } else {
-        encode_scalar<D, true><<<grid_for(encode_scalar<D, true>, blocks), kThreads, 0, s>>>(a);
+        encode_scalar<D, true, BLK><<<grid_for(encode_scalar<D, true, BLK>, blocks), kThreads, 0, s>>>(a);
     }
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_encode_d(const EncodeArgs& a, int dtype, bool vec, cudaStream_t s) {
+    return a.block_words ? launch_encode_db<D, true>(a, dtype, vec, s) : launch_encode_db<D, false>(a, dtype, vec, s);
 }
 
 }  // namespace

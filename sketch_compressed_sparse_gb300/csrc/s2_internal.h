@@ -37,6 +37,8 @@ struct EncodeArgs {
     uint32_t d;
     uint32_t w;
     RowKeys keys;
+    uint32_t block_words;  // 0: element bitmap; else one bit per block of this many bitmap words
+    uint64_t nbw;          // block bitmap words per worker (block mode)
 };
 
 // dtype: 0 = f32, 1 = bf16. vec: rows are 16-byte aligned (vector loads).
@@ -73,6 +75,7 @@ struct DecodeArgs {
     uint32_t w;
     float scale;
     RowKeys keys;
+    uint32_t block;  // 0: element bitmap; else a block bitmap, one bit per `block` positions
 };
 cudaError_t launch_decode_dense(const DecodeArgs& a, float* out, cudaStream_t s);
 
