@@ -26,6 +26,10 @@ Parity status of each function (what pins it, in ``tests/test_oracle_pins.py``):
   encode_blocks /    block bitmap = numpy any() over each block; block size 1
   decode_dense_blocks  equals the element functions; exact recovery of every
                      position of marked blocks (zeros included) without collisions
+  block_topk         kept blocks = numpy's lexsort (norm desc, index asc) of the
+                     oracle's norms; norms within fp32 rounding of float64
+                     norms; sparse + residual = grad + residual exactly; the
+                     delta-approximate bound of Theorem 2 (K/nb of the energy)
 All functions are pinned; none is "parity unpinned".
 """
 from __future__ import annotations
@@ -49,11 +53,13 @@ _DT = {"f32": 0, "bf16": 1}
 
 
 def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (plain -O2, no vectorisation flags)."""
+    """Compile the oracle with gcc (plain -O2; no contraction of a*b+c into fused
+    multiply-adds, so every float operation rounds as written)."""
     os.makedirs(_LIBDIR, exist_ok=True)
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC])
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, _SRC,
+                               "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -89,6 +95,8 @@ def _load():
         lib.s2o_encode_blocks.restype = None
         lib.s2o_decode_dense_blocks.argtypes = [vp, vp, vp, u64, u64, u32, u32, u32, dbl, vp, vp]
         lib.s2o_decode_dense_blocks.restype = None
+        lib.s2o_block_topk.argtypes = [vp, vp, u64, u64, u64, vp, vp, vp]
+        lib.s2o_block_topk.restype = None
         _lib = lib
         return lib
 
@@ -251,6 +259,22 @@ def pipeline_blocks(grad: np.ndarray, block: int, d: int, w: int, seed: int, dty
     bm, Ssum, Asum = reduce(bms, S, A)
     out, amax = decode_dense_blocks(bm, Ssum, n, block, seed, scale, Asum)
     return dict(bitmaps=bms, S=S, A=A, bitmap=bm, S_sum=Ssum, A_sum=Asum, out=out, amax=amax)
+
+
+def block_topk(grad: np.ndarray, residual: np.ndarray, block: int, K: int):
+    """Block-wise Top-K with error feedback for ONE worker (Section 2.2; Appendix A.2).
+
+    Returns (sparse float32[n], new residual float32[n], norms float32[nb], keep uint8[nb]).
+    """
+    g = np.ascontiguousarray(grad, dtype=np.float32)
+    e = np.array(residual, dtype=np.float32, copy=True)
+    n = g.size
+    nb = (n + block - 1) // block
+    sp = np.empty(n, dtype=np.float32)
+    nrm = np.empty(max(nb, 1), dtype=np.float32)
+    keep = np.empty(max(nb, 1), dtype=np.uint8)
+    _load().s2o_block_topk(_ptr(g), _ptr(e), n, block, K, _ptr(sp), _ptr(nrm), _ptr(keep))
+    return sp, e, nrm[:nb], keep[:nb]
 
 
 def encode_all(grad: np.ndarray, d: int, w: int, seed: int, dtype: str = "f32"):

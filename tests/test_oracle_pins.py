@@ -436,3 +436,60 @@ def test_block_decode_recovers_whole_blocks_exactly_without_collisions():
     np.testing.assert_array_equal(unpack_bits(res["bitmap"], n // block), [False, True] + [False] * 6 + [True] + [False] * 6 + [False])
     assert (res["out"][~marked] == 0).all()
     np.testing.assert_array_equal(res["out"][marked], G.sum(axis=0)[marked])
+
+
+# ----------------------------------------------------------------- block-wise Top-K + error feedback
+
+def _topk_case(n=10_000, block=64, tag=0):
+    rng = np.random.default_rng(tag)
+    g = rng.laplace(size=n).astype(np.float32)
+    e = (0.1 * rng.normal(size=n)).astype(np.float32)
+    return g, e
+
+
+@pytest.mark.parametrize("n,block,K", [(10_000, 64, 5), (10_000, 64, 0), (10_000, 64, 157), (1000, 96, 3),
+                                        (4096, 256, 1)])
+def test_block_topk_keeps_the_largest_blocks(n, block, K):
+    # Section 2.2: the K blocks with the largest l2 norms are kept
+    g, e = _topk_case(n, block, tag=K)
+    sp, e2, nrm, keep = oracle.block_topk(g, e, block, K)
+    acc = g + e  # float32 additions, as the method does
+    nb = (n + block - 1) // block
+    ref = np.zeros(nb)
+    for x in range(nb):
+        ref[x] = np.sum(acc[x * block:(x + 1) * block].astype(np.float64) ** 2)
+    np.testing.assert_allclose(nrm, ref, rtol=1e-5)  # the specified fp32 order stays close to float64
+    order = np.lexsort((np.arange(nb), -nrm.astype(np.float64)))
+    want = np.zeros(nb, dtype=np.uint8)
+    want[order[:K]] = 1
+    np.testing.assert_array_equal(keep, want)
+    kept = np.repeat(keep.astype(bool), block)[:n]
+    np.testing.assert_array_equal(sp, np.where(kept, acc, 0).astype(np.float32))
+    np.testing.assert_array_equal(sp + e2, acc)  # residual carries exactly what was not sent
+    assert (e2[kept] == 0).all()
+
+
+def test_block_topk_ties_go_to_the_lower_block():
+    g = np.ones(4 * 32, dtype=np.float32)  # four equal blocks
+    _, _, _, keep = oracle.block_topk(g, np.zeros_like(g), 32, 2)
+    np.testing.assert_array_equal(keep, [1, 1, 0, 0])
+
+
+def test_block_topk_is_a_delta_approximate_compressor():
+    # Theorem 2 / Appendix A.2: ||acc - sparse||^2 <= (1 - K/nb) ||acc||^2
+    g, e = _topk_case(20_000, 100, tag=7)
+    for K in (1, 10, 50, 199):
+        sp, _, _, _ = oracle.block_topk(g, e, 100, K)
+        acc = (g + e).astype(np.float64)
+        lost = np.sum((acc - sp) ** 2)
+        assert lost <= (1 - K / 200) * np.sum(acc ** 2) + 1e-9
+
+
+def test_block_topk_error_feedback_accumulates_what_was_dropped():
+    # two steps: the residual of step 1 joins the gradient of step 2
+    g1, _ = _topk_case(5000, 50, tag=1)
+    g2, _ = _topk_case(5000, 50, tag=2)
+    e0 = np.zeros(5000, dtype=np.float32)
+    sp1, e1, _, _ = oracle.block_topk(g1, e0, 50, 10)
+    sp2, e2, _, _ = oracle.block_topk(g2, e1, 50, 10)
+    np.testing.assert_allclose(sp1.astype(np.float64) + sp2 + e2, g1.astype(np.float64) + g2, atol=1e-5)
