@@ -429,6 +429,86 @@ def run_ours(args, wl, world, rank, local):
     return res
 
 
+def run_blocktopk(args, world, rank, local):
+    """Dense ResNet-50-size gradients -> block-wise Top-K (256-element blocks,
+    1/32 of the blocks kept, residual carried across steps) -> the per-worker
+    encode -> reduce -> decode path."""
+    import torch
+
+    import sketch_compressed_sparse_gb300 as s2
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    W, n, block, d, w, seed = 8, 25_557_032, 256, 3, 1 << 19, 0
+    nb = (n + block - 1) // block
+    K = nb // 32
+    grad = torch.from_numpy(workloads.dense_laplace(W, n)).to(dev)
+    resid = torch.zeros_like(grad)
+    sparse = torch.empty_like(grad)
+    ws = torch.empty(s2.s2_block_topk_workspace_size(W, n, block), dtype=torch.uint8, device=dev)
+    bitmaps = torch.empty((W, s2.nwords(n)), dtype=torch.int32, device=dev)
+    sketches = torch.empty((W, d, w), dtype=torch.float32, device=dev)
+    bitmap = torch.empty(s2.nwords(n), dtype=torch.int32, device=dev)
+    sketch = torch.empty((d, w), dtype=torch.float32, device=dev)
+    out = torch.empty(n, dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def stages(ev=None):
+        rec = (lambda i: ev[i].record(stream)) if ev else (lambda i: None)
+        rec(0)
+        s2.s2_block_topk(grad, resid, block, K, sparse, ws)
+        rec(1)
+        s2.s2_encode_batched(sparse, d, w, seed, bitmaps, sketches)
+        rec(2)
+        s2.s2_reduce(bitmaps, sketches, n, d, w, bitmap, sketch)
+        rec(3)
+        s2.s2_decode_dense(bitmap, sketch, n, d, w, seed, out)
+        rec(4)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        stages()
+    Ksteps = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(Ksteps)]
+    torch.cuda.synchronize(dev)
+    with ClockSampler(physical_gpu_index(local)) as clk:
+        for k in range(Ksteps):
+            flush.fill_(float(k & 7))
+            stages(evs[k])
+        torch.cuda.synchronize(dev)
+    t = [sum(e[i].elapsed_time(e[i + 1]) for e in evs) / Ksteps for i in range(4)]
+    step_ms = sum(t)
+    union = int((torch.from_numpy(np.unpackbits(bitmap.cpu().numpy().view(np.uint8), bitorder="little")[:n])).sum())
+    peak = measured_peaks()["hbm_gbs"]
+    topk_bytes = W * n * 16  # read grad and residual, write sparse output and residual
+    SK, BM = 4 * d * w, 4 * ((n + 31) // 32)
+    enc_b, red_b = W * n * 4 + W * BM + W * SK, W * (SK + BM) + SK + BM
+    dec_b = BM + min(SK, 4 * d * union) + 4 * n
+    total_b = topk_bytes + enc_b + red_b + dec_b
+    return {
+        "metric": METRIC, "value": round(W * n / (step_ms / 1e3) / 1e9, 3), "unit": "Gelem/s", "n_gpus": world,
+        "steps": Ksteps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "block_topk_resnet50", "W": W, "n": n, "block": block, "K": K, "d": d, "w": w,
+                   "hash_seed": seed, "nnz_union_last_step": union,
+                   "mode": "block-wise Top-K with error feedback, then the per-worker path",
+                   "l2": "flushed before every step (512 MiB write)"},
+        "stages_ms_per_step": {"block_topk": round(t[0], 5), "encode": round(t[1], 5), "reduce": round(t[2], 5),
+                               "decode": round(t[3], 5)},
+        "roofline": {"kernel": "block_topk (norms + select + apply)", "bound": "hbm",
+                     "achieved": round(topk_bytes / (t[0] / 1e3) / 1e9, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(topk_bytes / (t[0] / 1e3) / 1e9 / peak, 4), "traffic": None,
+                     "algorithmic_bytes_per_step": topk_bytes},
+        "path_roofline": {"bound": "hbm", "achieved": round(total_b / (step_ms / 1e3) / 1e9, 1), "peak": peak,
+                          "unit": "GB/s", "frac": round(total_b / (step_ms / 1e3) / 1e9 / peak, 4),
+                          "algorithmic_bytes_per_step": total_b},
+        "gpu_launches": Ksteps * (3 + encode_launches(workloads.Workload("x", W, n, d, w, 0, "f32", [], []),
+                                                      int(torch.cuda.get_device_properties(dev).L2_cache_size)) + 2),
+        "clocks": clk.summary(),
+    }
+
+
 def run_e2e(args, wl, dev, s2):
     """Host pinned grad -> device -> path -> host out, through s2_pipeline_dense_host."""
     import torch
@@ -522,7 +602,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="embedding", choices=["tiny", "embedding", "topk", "large_lm"])
+    ap.add_argument("--config", default="embedding", choices=["tiny", "embedding", "topk", "large_lm", "blocktopk"])
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle timing")
     ap.add_argument("--e2e-steps", type=int, default=20)
@@ -545,7 +625,10 @@ def main(argv=None):
     if args.impl == "reference":
         if rank != 0:
             return 0
-        res = run_reference(args, workloads.by_name(args.config))
+        if args.config == "blocktopk":
+            res = {"impl": "reference", "unavailable": "the CPU reference arm covers the four S2 workloads only"}
+        else:
+            res = run_reference(args, workloads.by_name(args.config))
     else:
         if world > 1:
             import torch
@@ -553,7 +636,10 @@ def main(argv=None):
 
             torch.cuda.set_device(local)
             dist.init_process_group("nccl")
-        res = run_ours(args, select_workers(workloads.by_name(args.config), args.workers), world, rank, local)
+        if args.config == "blocktopk":
+            res = run_blocktopk(args, world, rank, local)
+        else:
+            res = run_ours(args, select_workers(workloads.by_name(args.config), args.workers), world, rank, local)
         if world > 1:
             import torch.distributed as dist
 

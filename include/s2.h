@@ -123,6 +123,29 @@ S2_API s2_status s2_encode_batched_blocks(const void *grad, s2_dtype dt, uint32_
                                           s2_stream_t stream);
 
 /*
+ * s2_block_topk -- block-wise Top-K sparsification with error feedback, the
+ * step before encode in the paper's second setting (Section 2.2 "Sparse
+ * Gradient & AllGather": keep the K blocks of largest l2 norm; Appendix A.2:
+ * the residual e_{t+1} = g_t - U(g_t) joins the next step's gradient).
+ *   grad [W][n] float32 in; residual [W][n] float32 in/out (zeros at the
+ *   first step); sparse_out [W][n] float32 out. Per worker: acc = grad +
+ *   residual; the squared norm of every block of `block` elements (the last
+ *   one may be shorter) is summed in float32 in a fixed order (lane l of 32
+ *   accumulates fmaf(a, a, s) over elements l, l+32, ...; then an XOR
+ *   butterfly over the 32 partials, offsets 16, 8, 4, 2, 1); the K blocks of
+ *   largest norm are kept, ties going to the lower block index;
+ *   sparse_out = acc on kept blocks and 0 elsewhere, residual = acc elsewhere
+ *   and 0 on kept blocks.
+ *   block: a multiple of 32 (S2_ERR_UNSUPPORTED otherwise); K <= ceil(n/block)
+ *   (S2_ERR_INVALID_ARG otherwise). workspace: s2_block_topk_workspace_size
+ *   bytes, 16-byte aligned, contents on entry irrelevant.
+ */
+S2_API s2_status s2_block_topk_workspace_size(uint32_t W, uint64_t n, uint32_t block, size_t *bytes);
+S2_API s2_status s2_block_topk(const float *grad, float *residual, uint32_t W, uint64_t n, uint32_t block,
+                               uint64_t K, float *sparse_out, void *workspace, size_t workspace_bytes,
+                               s2_stream_t stream);
+
+/*
  * s2_reduce -- the AllReduce(S, C) of Algorithm 1 (Section 3.1 "Collecting
  * Sparse-Sketch with AllReduce"), with all W workers resident on this GPU.
  *   bitmaps [W][nw], sketches [W][d][w]  in.

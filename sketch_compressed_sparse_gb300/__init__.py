@@ -27,6 +27,8 @@ __all__ = [
     "s2_reduce",
     "s2_encode_reduce_fused",
     "s2_encode_batched_blocks",
+    "s2_block_topk",
+    "s2_block_topk_workspace_size",
     "s2_decode_dense_blocks",
     "s2_decode_dense",
     "s2_decode_workspace_size",
@@ -62,6 +64,8 @@ _SIGS = {
     "s2_reduce": ([_vp, _vp, _u32, _u64, Params, _vp, _vp, _vp], _i32),
     "s2_encode_reduce_fused": ([_vp, _i32, _u32, _u64, Params, _vp, _vp, _vp], _i32),
     "s2_encode_batched_blocks": ([_vp, _i32, _u32, _u64, _u32, Params, _vp, _vp, _vp], _i32),
+    "s2_block_topk_workspace_size": ([_u32, _u64, _u32, ctypes.POINTER(_sz)], _i32),
+    "s2_block_topk": ([_vp, _vp, _u32, _u64, _u32, _u64, _vp, _vp, _sz, _vp], _i32),
     "s2_decode_dense_blocks": ([_vp, _vp, _u64, _u32, Params, _f32, _vp, _vp], _i32),
     "s2_decode_dense": ([_vp, _vp, _u64, Params, _f32, _vp, _vp], _i32),
     "s2_decode_workspace_size": ([_u64, ctypes.POINTER(_sz)], _i32),
@@ -201,6 +205,25 @@ def s2_encode_reduce_fused(grad: torch.Tensor, d: int, w: int, seed: int, bitmap
                                         _dev(bitmap_out, "bitmap_out", _U32, nwords(n)),
                                         _dev(sketch_out, "sketch_out", (torch.float32,), d * w), _stream(stream)),
            "s2_encode_reduce_fused")
+
+
+def s2_block_topk_workspace_size(W: int, n: int, block: int) -> int:
+    b = _sz()
+    _check(_f("s2_block_topk_workspace_size")(W, n, block, ctypes.byref(b)), "s2_block_topk_workspace_size")
+    return int(b.value)
+
+
+def s2_block_topk(grad: torch.Tensor, residual: torch.Tensor, block: int, K: int, sparse_out: torch.Tensor,
+                  workspace: torch.Tensor, stream=None) -> None:
+    """Block-wise Top-K with error feedback: grad [W, n], residual [W, n] (in/out) -> sparse_out [W, n]."""
+    if grad.dim() != 2:
+        raise ValueError("grad must be [W, n]")
+    W, n = grad.shape
+    _check(_f("s2_block_topk")(_dev(grad, "grad", (torch.float32,), W * n),
+                               _dev(residual, "residual", (torch.float32,), W * n), W, n, block, K,
+                               _dev(sparse_out, "sparse_out", (torch.float32,), W * n),
+                               _dev(workspace, "workspace", (torch.uint8,)), workspace.numel(), _stream(stream)),
+           "s2_block_topk")
 
 
 def nblockwords(n: int, block: int) -> int:

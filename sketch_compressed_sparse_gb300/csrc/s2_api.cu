@@ -266,6 +266,31 @@ s2_status s2_decode_dense_blocks(const uint32_t* block_bitmap, const float* sket
     return cuda_status(launch_decode_dense(a, out, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+s2_status s2_block_topk_workspace_size(uint32_t W, uint64_t n, uint32_t block, size_t* bytes) {
+    if (!bytes) return S2_ERR_INVALID_ARG;
+    if (block == 0 || block % 32 != 0 || n > kMaxN) return S2_ERR_UNSUPPORTED;
+    *bytes = topk_workspace_bytes(W, n, block);
+    return S2_OK;
+}
+
+s2_status s2_block_topk(const float* grad, float* residual, uint32_t W, uint64_t n, uint32_t block, uint64_t K,
+                        float* sparse_out, void* workspace, size_t workspace_bytes, s2_stream_t stream) {
+    if (block == 0 || block % 32 != 0 || n > kMaxN) return S2_ERR_UNSUPPORTED;
+    const uint64_t nb = (n + block - 1) / block, bytes = (uint64_t)W * n * 4;
+    if (K > nb) return S2_ERR_INVALID_ARG;
+    if (bytes == 0) return S2_OK;
+    const size_t need = topk_workspace_bytes(W, n, block);
+    if (!grad || !residual || !sparse_out || !workspace || workspace_bytes < need) return S2_ERR_INVALID_ARG;
+    if (!aligned(grad, 16) || !aligned(residual, 16) || !aligned(sparse_out, 16) || !aligned(workspace, 16))
+        return S2_ERR_ALIGNMENT;
+    if (overlap(grad, bytes, residual, bytes) || overlap(grad, bytes, sparse_out, bytes) ||
+        overlap(residual, bytes, sparse_out, bytes) || overlap(workspace, need, grad, bytes) ||
+        overlap(workspace, need, residual, bytes) || overlap(workspace, need, sparse_out, bytes))
+        return S2_ERR_INVALID_ARG;
+    return cuda_status(
+        launch_block_topk(grad, residual, W, n, block, K, sparse_out, workspace, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 s2_status s2_reduce(const uint32_t* bitmaps, const float* sketches, uint32_t W, uint64_t n, s2_params p,
                     uint32_t* bitmap_out, float* sketch_out, s2_stream_t stream) {
     s2_status st = check_reduce(bitmaps, sketches, W, n, p, bitmap_out, sketch_out);

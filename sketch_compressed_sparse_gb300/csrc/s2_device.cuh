@@ -61,6 +61,8 @@ __device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
     return r;
 }
 
+__device__ __forceinline__ float ld_stream_f32(const float* p) { return __uint_as_float(ld_stream_u32(p)); }
+
 __device__ __forceinline__ uint16_t ld_stream_u16(const void* p) {
     uint16_t r;
     asm("ld.global.cs.u16 %0, [%1];" : "=h"(r) : "l"(p));

@@ -61,6 +61,11 @@ struct FusedArgs {
 // Zero-fills the sketch, then one pass over all workers (dtype: 0 f32, 1 bf16).
 cudaError_t launch_fused(const FusedArgs& a, int dtype, cudaStream_t s);
 
+// ---- block-wise Top-K with error feedback (upstream of encode) -------------
+size_t topk_workspace_bytes(uint32_t W, uint64_t n, uint32_t block);
+cudaError_t launch_block_topk(const float* grad, float* resid, uint32_t W, uint64_t n, uint32_t block, uint64_t K,
+                              float* sparse, void* workspace, cudaStream_t s);
+
 // ---- reduce ----------------------------------------------------------------
 cudaError_t launch_reduce(const uint32_t* bitmaps, const float* sketches, uint32_t W, uint64_t nw,
                           uint64_t dw, uint32_t* bitmap_out, float* sketch_out, cudaStream_t s);

@@ -32,6 +32,7 @@ __all__ = [
     "large_lm",
     "sweep_point",
     "sweep_grid",
+    "dense_laplace",
     "by_name",
     "custom",
     "f32_to_bf16_bits",
@@ -354,6 +355,16 @@ def random_bitmaps(W: int, n: int, density: float, tag: int = 12) -> np.ndarray:
     for k in range(W):
         pos = _uniform_positions(rng, n, int(round(density * n)))
         np.bitwise_or.at(out[k], pos >> 5, (np.uint32(1) << (pos & 31).astype(np.uint32)))
+    return out
+
+
+def dense_laplace(W: int = 8, n: int = 25_557_032, tag: int = 1005) -> np.ndarray:
+    """Dense float32 gradients [W][n] of Laplace(0,1) draws (ResNet-50 size),
+    the input of the block-wise Top-K sparsifier (one draw per worker)."""
+    ch = _children(tag, W)
+    out = np.empty((W, n), dtype=np.float32)
+    for k in range(W):
+        out[k] = np.random.default_rng(ch[k]).laplace(0.0, 1.0, size=n).astype(np.float32)
     return out
 
 
