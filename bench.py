@@ -133,12 +133,12 @@ def measured_peaks() -> dict:
 
 
 def kernel_source_sha() -> str:
+    """Hash of the sources that define the encode stage (its kernels and their helpers)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sketch_compressed_sparse_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+    for f in ("s2_device.cuh", "s2_internal.h", "s2_encode.cu"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
