@@ -30,6 +30,9 @@ Parity status of each function (what pins it, in ``tests/test_oracle_pins.py``):
                      oracle's norms; norms within fp32 rounding of float64
                      norms; sparse + residual = grad + residual exactly; the
                      delta-approximate bound of Theorem 2 (K/nb of the energy)
+  sparse_list /      indices = numpy flatnonzero of the bit test, capacity keeps
+  exact_sum          the true count; exact_sum = float64 numpy sum; equals the
+                     S2 decode wherever no row collides
 All functions are pinned; none is "parity unpinned".
 """
 from __future__ import annotations
@@ -95,6 +98,10 @@ def _load():
         lib.s2o_encode_blocks.restype = None
         lib.s2o_decode_dense_blocks.argtypes = [vp, vp, vp, u64, u64, u32, u32, u32, dbl, vp, vp]
         lib.s2o_decode_dense_blocks.restype = None
+        lib.s2o_sparse_list.argtypes = [vp, u64, vp, vp, u64]
+        lib.s2o_sparse_list.restype = u64
+        lib.s2o_exact_sum.argtypes = [vp, u32, u64, vp]
+        lib.s2o_exact_sum.restype = None
         lib.s2o_block_topk.argtypes = [vp, vp, u64, u64, u64, vp, vp, vp]
         lib.s2o_block_topk.restype = None
         _lib = lib
@@ -275,6 +282,26 @@ def block_topk(grad: np.ndarray, residual: np.ndarray, block: int, K: int):
     keep = np.empty(max(nb, 1), dtype=np.uint8)
     _load().s2o_block_topk(_ptr(g), _ptr(e), n, block, K, _ptr(sp), _ptr(nrm), _ptr(keep))
     return sp, e, nrm[:nb], keep[:nb]
+
+
+def sparse_list(grad: np.ndarray, capacity: Optional[int] = None):
+    """AllGather baseline message of one worker: (count, idx uint32[...], val float32[...]) ascending."""
+    g = np.ascontiguousarray(grad, dtype=np.float32)
+    cap = g.size if capacity is None else capacity
+    idx = np.empty(max(cap, 1), dtype=np.uint32)
+    val = np.empty(max(cap, 1), dtype=np.float32)
+    c = int(_load().s2o_sparse_list(_ptr(g), g.size, _ptr(idx), _ptr(val), cap))
+    m = min(c, cap)
+    return c, idx[:m].copy(), val[:m].copy()
+
+
+def exact_sum(grads: np.ndarray) -> np.ndarray:
+    """The gathered lists added up (float64 accumulation, one rounding): float32[n]."""
+    g = np.ascontiguousarray(grads, dtype=np.float32)
+    W, n = g.shape
+    out = np.empty(n, dtype=np.float32)
+    _load().s2o_exact_sum(_ptr(g), W, n, _ptr(out))
+    return out
 
 
 def encode_all(grad: np.ndarray, d: int, w: int, seed: int, dtype: str = "f32"):

@@ -415,3 +415,37 @@ void s2o_block_topk(const float *grad, float *residual, uint64_t n, uint64_t blo
     free(nrm);
     free(keep);
 }
+
+/* ---- sparse AllGather baseline -------------------------------------------- */
+
+/*
+ * Section 2.2 "Sparse Gradient & AllGather" / Figure 1(b): a worker's message
+ * is the list of its nonzero indices and values (ascending); entries at
+ * t >= capacity are not written. Returns the number of nonzeros.
+ */
+uint64_t s2o_sparse_list(const float *grad, uint64_t n, uint32_t *idx, float *val, uint64_t capacity)
+{
+    uint64_t t = 0;
+    for (uint64_t i = 0; i < n; ++i) {
+        if (!elem_is_nonzero(grad, 0, i))
+            continue;
+        if (t < capacity) {
+            idx[t] = (uint32_t)i;
+            val[t] = grad[i];
+        }
+        ++t;
+    }
+    return t;
+}
+
+/* The gathered lists added up: out[i] = sum over workers of their value at i
+ * (double accumulation, rounded once). grads: W x n. */
+void s2o_exact_sum(const float *grads, uint32_t W, uint64_t n, float *out)
+{
+    for (uint64_t i = 0; i < n; ++i) {
+        double s = 0.0;
+        for (uint32_t k = 0; k < W; ++k)
+            s += (double)grads[(uint64_t)k * n + i];
+        out[i] = (float)s;
+    }
+}

@@ -493,3 +493,31 @@ def test_block_topk_error_feedback_accumulates_what_was_dropped():
     sp1, e1, _, _ = oracle.block_topk(g1, e0, 50, 10)
     sp2, e2, _, _ = oracle.block_topk(g2, e1, 50, 10)
     np.testing.assert_allclose(sp1.astype(np.float64) + sp2 + e2, g1.astype(np.float64) + g2, atol=1e-5)
+
+
+# ----------------------------------------------------------------- sparse AllGather baseline
+
+def test_sparse_list_is_the_ascending_support():
+    g = np.zeros(3000, dtype=np.float32)
+    pos = np.array([3, 40, 41, 2999])
+    g[pos] = [1.5, -2.0, 1e-45, 7.0]
+    g[100] = np.float32(-0.0)
+    c, idx, val = oracle.sparse_list(g)
+    assert c == 4
+    np.testing.assert_array_equal(idx, pos.astype(np.uint32))
+    np.testing.assert_array_equal(val, g[pos])
+    c2, idx2, _ = oracle.sparse_list(g, capacity=2)
+    assert c2 == 4 and idx2.size == 2
+
+
+def test_exact_sum_and_agreement_with_the_sketch_without_collisions():
+    wl = workloads.custom(W=4, n=20_000, d=3, w=1 << 20, density=0.002, values="int", tag=91)
+    G = wl.dense()
+    ex = oracle.exact_sum(G)
+    np.testing.assert_array_equal(ex, G.astype(np.float64).sum(axis=0).astype(np.float32))
+    res = oracle.pipeline(G, wl.d, wl.w, wl.seed)
+    union = (G != 0).any(axis=0)
+    free = _union_collision_free_rows(np.flatnonzero(union), wl.d, wl.w, wl.seed)
+    good = np.flatnonzero(union)[free == wl.d]
+    assert good.size > 0.95 * union.sum()
+    np.testing.assert_array_equal(res["out"][good], ex[good])
