@@ -509,6 +509,82 @@ def run_blocktopk(args, world, rank, local):
     }
 
 
+def run_allgather(args, wl, world, rank, local):
+    """The sparse AllGather baseline on the same workload: pack every worker's
+    (index, value) list, sum the gathered lists; beside it the bytes each
+    worker would send with either method and the S2 decode's error against
+    this exact aggregate."""
+    import torch
+
+    import sketch_compressed_sparse_gb300 as s2
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    W, n, d, w, seed = wl.W, wl.n, wl.d, wl.w, wl.seed
+    if wl.dtype != "f32":
+        raise SystemExit("the AllGather baseline takes float32 gradients")
+    cap = max(wl.nnz_per_worker)
+    grad = wl.dense_torch(dev)
+    idx = torch.empty((W, cap), dtype=torch.int32, device=dev)
+    val = torch.empty((W, cap), dtype=torch.float32, device=dev)
+    cnt = torch.empty(W, dtype=torch.int64, device=dev)
+    ws = torch.empty(s2.s2_sparse_pack_workspace_size(W, n), dtype=torch.uint8, device=dev)
+    exact = torch.empty(n, dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        s2.s2_sparse_pack(grad, idx, val, cnt, ws)
+        s2.s2_sparse_sum(idx, val, cnt, n, exact)
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    torch.cuda.synchronize(dev)
+    with ClockSampler(physical_gpu_index(local)) as clk:
+        for k in range(K):
+            flush.fill_(float(k & 7))
+            e = evs[k]
+            e[0].record(stream)
+            s2.s2_sparse_pack(grad, idx, val, cnt, ws)
+            e[1].record(stream)
+            s2.s2_sparse_sum(idx, val, cnt, n, exact)
+            e[2].record(stream)
+        torch.cuda.synchronize(dev)
+    pack_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / K
+    sum_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / K
+    # the S2 path once, untimed, for its error against the exact aggregate
+    bitmaps, sketches = s2.alloc_encode_outputs(W, n, d, w, dev)
+    bitmap = torch.empty(s2.nwords(n), dtype=torch.int32, device=dev)
+    sketch = torch.empty((d, w), dtype=torch.float32, device=dev)
+    out = torch.empty(n, dtype=torch.float32, device=dev)
+    s2.s2_encode_batched(grad, d, w, seed, bitmaps, sketches)
+    s2.s2_reduce(bitmaps, sketches, n, d, w, bitmap, sketch)
+    s2.s2_decode_dense(bitmap, sketch, n, d, w, seed, out)
+    torch.cuda.synchronize(dev)
+    err = (out.double() - exact.double()).norm().item() / max(exact.double().norm().item(), 1e-300)
+    nnz = [int(c) for c in cnt.cpu().tolist()]
+    bytes_ag = 8 * sum(nnz) // W
+    bytes_s2 = 4 * d * w + 4 * ((n + 31) // 32)
+    peak = measured_peaks()["hbm_gbs"]
+    alg = W * n * 4 + 2 * 8 * sum(nnz) + 4 * n  # read grads, write + read the lists, write the sum
+    step_ms = pack_ms + sum_ms
+    return {
+        "metric": METRIC, "value": round(W * n / (step_ms / 1e3) / 1e9, 3), "unit": "Gelem/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": dict(wl.describe(), mode="sparse AllGather baseline (pack + sum), exact aggregate",
+                       l2="flushed before every step (512 MiB write)"),
+        "stages_ms_per_step": {"pack": round(pack_ms, 5), "sum": round(sum_ms, 5)},
+        "path_roofline": {"bound": "hbm", "achieved": round(alg / (step_ms / 1e3) / 1e9, 1), "peak": peak,
+                          "unit": "GB/s", "frac": round(alg / (step_ms / 1e3) / 1e9 / peak, 4),
+                          "algorithmic_bytes_per_step": alg},
+        "message_bytes_per_worker": {"allgather_lists": bytes_ag, "s2_sketch_and_bitmap": bytes_s2,
+                                     "ratio_s2_over_allgather": round(bytes_s2 / max(bytes_ag, 1), 4)},
+        "s2_decode_rel_l2_error_vs_exact": err,
+        "gpu_launches": K * (2 + W + 1 + W),
+        "clocks": clk.summary(),
+    }
+
+
 def run_e2e(args, wl, dev, s2):
     """Host pinned grad -> device -> path -> host out, through s2_pipeline_dense_host."""
     import torch
@@ -607,8 +683,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle timing")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
-    ap.add_argument("--mode", choices=["per_worker", "fused"], default="per_worker",
-                    help="per_worker: the simulated data-parallel path (default); fused: encode_reduce_fused + decode")
+    ap.add_argument("--mode", choices=["per_worker", "fused", "allgather"], default="per_worker",
+                    help="per_worker: the simulated data-parallel path (default); fused: encode_reduce_fused + "
+                         "decode; allgather: the sparse AllGather baseline (exact sum) on the same workload")
     ap.add_argument("--block", type=int, default=0,
                     help="positions per bitmap bit (a multiple of 32; 0 = one bit per position, the default)")
     ap.add_argument("--workers", type=int, default=None,
@@ -638,6 +715,8 @@ def main(argv=None):
             dist.init_process_group("nccl")
         if args.config == "blocktopk":
             res = run_blocktopk(args, world, rank, local)
+        elif args.mode == "allgather":
+            res = run_allgather(args, workloads.by_name(args.config), world, rank, local)
         else:
             res = run_ours(args, select_workers(workloads.by_name(args.config), args.workers), world, rank, local)
         if world > 1:

@@ -146,6 +146,27 @@ S2_API s2_status s2_block_topk(const float *grad, float *residual, uint32_t W, u
                                s2_stream_t stream);
 
 /*
+ * s2_sparse_pack / s2_sparse_sum -- the sparse AllGather baseline the paper
+ * compares S2 Reducer with (Section 2.2 "Sparse Gradient & AllGather" and
+ * Figure 1(b)): each worker sends the indices and values of its nonzeros,
+ * every worker gathers all the lists and adds them up. Here, on one GPU:
+ *   s2_sparse_pack: grad [W][n] float32 in; idx_out [W][capacity] uint32 and
+ *   val_out [W][capacity] float32 out, worker k's nonzeros (bit pattern test
+ *   as in s2_encode) in ascending index order; counts_out [W] uint64 (device)
+ *   receives each worker's true count (entries past capacity are not
+ *   written). workspace: s2_sparse_pack_workspace_size bytes, 16-byte aligned.
+ *   s2_sparse_sum: out [n] float32 = the sum of all W lists, added in worker
+ *   order 0..W-1 (the exact aggregate the sketch approximates; bit-identical
+ *   to a sequential float32 sum over workers). Indices >= n are skipped.
+ */
+S2_API s2_status s2_sparse_pack_workspace_size(uint32_t W, uint64_t n, size_t *bytes);
+S2_API s2_status s2_sparse_pack(const float *grad, uint32_t W, uint64_t n, uint32_t *idx_out, float *val_out,
+                                uint64_t capacity, uint64_t *counts_out, void *workspace, size_t workspace_bytes,
+                                s2_stream_t stream);
+S2_API s2_status s2_sparse_sum(const uint32_t *idx, const float *val, const uint64_t *counts, uint32_t W,
+                               uint64_t capacity, uint64_t n, float *out, s2_stream_t stream);
+
+/*
  * s2_reduce -- the AllReduce(S, C) of Algorithm 1 (Section 3.1 "Collecting
  * Sparse-Sketch with AllReduce"), with all W workers resident on this GPU.
  *   bitmaps [W][nw], sketches [W][d][w]  in.

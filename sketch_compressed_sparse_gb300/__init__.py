@@ -28,6 +28,8 @@ __all__ = [
     "s2_encode_reduce_fused",
     "s2_encode_batched_blocks",
     "s2_block_topk",
+    "s2_sparse_pack",
+    "s2_sparse_sum",
     "s2_block_topk_workspace_size",
     "s2_decode_dense_blocks",
     "s2_decode_dense",
@@ -65,6 +67,9 @@ _SIGS = {
     "s2_encode_reduce_fused": ([_vp, _i32, _u32, _u64, Params, _vp, _vp, _vp], _i32),
     "s2_encode_batched_blocks": ([_vp, _i32, _u32, _u64, _u32, Params, _vp, _vp, _vp], _i32),
     "s2_block_topk_workspace_size": ([_u32, _u64, _u32, ctypes.POINTER(_sz)], _i32),
+    "s2_sparse_pack_workspace_size": ([_u32, _u64, ctypes.POINTER(_sz)], _i32),
+    "s2_sparse_pack": ([_vp, _u32, _u64, _vp, _vp, _u64, _vp, _vp, _sz, _vp], _i32),
+    "s2_sparse_sum": ([_vp, _vp, _vp, _u32, _u64, _u64, _vp, _vp], _i32),
     "s2_block_topk": ([_vp, _vp, _u32, _u64, _u32, _u64, _vp, _vp, _sz, _vp], _i32),
     "s2_decode_dense_blocks": ([_vp, _vp, _u64, _u32, Params, _f32, _vp, _vp], _i32),
     "s2_decode_dense": ([_vp, _vp, _u64, Params, _f32, _vp, _vp], _i32),
@@ -224,6 +229,33 @@ def s2_block_topk(grad: torch.Tensor, residual: torch.Tensor, block: int, K: int
                                _dev(sparse_out, "sparse_out", (torch.float32,), W * n),
                                _dev(workspace, "workspace", (torch.uint8,)), workspace.numel(), _stream(stream)),
            "s2_block_topk")
+
+
+def s2_sparse_pack_workspace_size(W: int, n: int) -> int:
+    b = _sz()
+    _check(_f("s2_sparse_pack_workspace_size")(W, n, ctypes.byref(b)), "s2_sparse_pack_workspace_size")
+    return int(b.value)
+
+
+def s2_sparse_pack(grad: torch.Tensor, idx_out: torch.Tensor, val_out: torch.Tensor, counts_out: torch.Tensor,
+                   workspace: torch.Tensor, stream=None) -> None:
+    """AllGather baseline, pack: grad [W, n] -> idx_out/val_out [W, cap] (ascending), counts_out [W] int64."""
+    W, n = grad.shape
+    cap = idx_out.shape[1] if idx_out.dim() == 2 else 0
+    _check(_f("s2_sparse_pack")(_dev(grad, "grad", (torch.float32,), W * n), W, n,
+                                _dev(idx_out, "idx_out", _U32, W * cap), _dev(val_out, "val_out", (torch.float32,), W * cap),
+                                cap, _dev(counts_out, "counts_out", (torch.int64,), W),
+                                _dev(workspace, "workspace", (torch.uint8,)), workspace.numel(), _stream(stream)),
+           "s2_sparse_pack")
+
+
+def s2_sparse_sum(idx: torch.Tensor, val: torch.Tensor, counts: torch.Tensor, n: int, out: torch.Tensor,
+                  stream=None) -> None:
+    """AllGather baseline, sum: the W gathered lists -> out [n] (worker order 0..W-1)."""
+    W, cap = idx.shape
+    _check(_f("s2_sparse_sum")(_dev(idx, "idx", _U32, W * cap), _dev(val, "val", (torch.float32,), W * cap),
+                               _dev(counts, "counts", (torch.int64,), W), W, cap, n,
+                               _dev(out, "out", (torch.float32,), n), _stream(stream)), "s2_sparse_sum")
 
 
 def nblockwords(n: int, block: int) -> int:

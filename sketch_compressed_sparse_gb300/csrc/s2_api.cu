@@ -291,6 +291,51 @@ s2_status s2_block_topk(const float* grad, float* residual, uint32_t W, uint64_t
         launch_block_topk(grad, residual, W, n, block, K, sparse_out, workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+s2_status s2_sparse_pack_workspace_size(uint32_t W, uint64_t n, size_t* bytes) {
+    if (!bytes) return S2_ERR_INVALID_ARG;
+    if (n > kMaxN) return S2_ERR_UNSUPPORTED;
+    *bytes = pack_workspace_bytes(W, n);
+    return S2_OK;
+}
+
+s2_status s2_sparse_pack(const float* grad, uint32_t W, uint64_t n, uint32_t* idx_out, float* val_out,
+                         uint64_t capacity, uint64_t* counts_out, void* workspace, size_t workspace_bytes,
+                         s2_stream_t stream) {
+    if (n > kMaxN) return S2_ERR_UNSUPPORTED;
+    if (W == 0) return S2_OK;
+    const size_t need = pack_workspace_bytes(W, n);
+    const uint64_t gbytes = (uint64_t)W * n * 4, lbytes = (uint64_t)W * capacity * 4;
+    if (!counts_out || (n > 0 && (!grad || !workspace || workspace_bytes < need)) ||
+        (capacity > 0 && (!idx_out || !val_out)))
+        return S2_ERR_INVALID_ARG;
+    if (!aligned(grad, 16) || !aligned(idx_out, 4) || !aligned(val_out, 4) || !aligned(counts_out, 8) ||
+        !aligned(workspace, 16))
+        return S2_ERR_ALIGNMENT;
+    const void* outs[4] = {idx_out, val_out, counts_out, workspace};
+    const uint64_t osz[4] = {lbytes, lbytes, (uint64_t)W * 8, need};
+    for (int o = 0; o < 4; ++o) {
+        if (overlap(grad, gbytes, outs[o], osz[o])) return S2_ERR_INVALID_ARG;
+        for (int q = o + 1; q < 4; ++q)
+            if (overlap(outs[o], osz[o], outs[q], osz[q])) return S2_ERR_INVALID_ARG;
+    }
+    return cuda_status(launch_sparse_pack(grad, W, n, idx_out, val_out, capacity,
+                                          reinterpret_cast<unsigned long long*>(counts_out), workspace,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+s2_status s2_sparse_sum(const uint32_t* idx, const float* val, const uint64_t* counts, uint32_t W, uint64_t capacity,
+                        uint64_t n, float* out, s2_stream_t stream) {
+    if (n > kMaxN) return S2_ERR_UNSUPPORTED;
+    if (n == 0) return S2_OK;
+    const uint64_t lbytes = (uint64_t)W * capacity * 4;
+    if (!out || (W > 0 && (!counts || (capacity > 0 && (!idx || !val))))) return S2_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(idx, 4) || !aligned(val, 4) || !aligned(counts, 8)) return S2_ERR_ALIGNMENT;
+    if (overlap(out, n * 4, idx, lbytes) || overlap(out, n * 4, val, lbytes) || overlap(out, n * 4, counts, W * 8ull))
+        return S2_ERR_INVALID_ARG;
+    return cuda_status(launch_sparse_sum(idx, val, reinterpret_cast<const unsigned long long*>(counts), W, capacity, n,
+                                         out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 s2_status s2_reduce(const uint32_t* bitmaps, const float* sketches, uint32_t W, uint64_t n, s2_params p,
                     uint32_t* bitmap_out, float* sketch_out, s2_stream_t stream) {
     s2_status st = check_reduce(bitmaps, sketches, W, n, p, bitmap_out, sketch_out);

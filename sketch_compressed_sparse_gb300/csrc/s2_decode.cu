@@ -327,6 +327,12 @@ cudaError_t launch_decode_dense(const DecodeArgs& a, float* out, cudaStream_t s)
     }
 }
 
+cudaError_t launch_tile_scan(const uint32_t* counts, uint64_t tiles, uint32_t* offsets, unsigned long long* total,
+                             cudaStream_t s) {
+    compact_scan_kernel<<<1, kScanThreads, 0, s>>>(counts, tiles, offsets, total);
+    return cudaGetLastError();
+}
+
 uint64_t compact_tiles(uint64_t nw) { return (nw + kCompactTileWords - 1) / kCompactTileWords; }
 
 size_t compact_workspace_bytes(uint64_t n) {

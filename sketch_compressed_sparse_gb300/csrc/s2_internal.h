@@ -91,6 +91,17 @@ cudaError_t launch_decode_compact(const DecodeArgs& a, uint32_t* idx_out, float*
                                   uint64_t capacity, unsigned long long* count_out,
                                   uint32_t* tile_counts, uint32_t* tile_offsets, cudaStream_t s);
 
+// Exclusive scan of `tiles` 32-bit counts by one block; *total gets the sum.
+cudaError_t launch_tile_scan(const uint32_t* counts, uint64_t tiles, uint32_t* offsets, unsigned long long* total,
+                             cudaStream_t s);
+
+// ---- sparse AllGather baseline ---------------------------------------------
+size_t pack_workspace_bytes(uint32_t W, uint64_t n);
+cudaError_t launch_sparse_pack(const float* grad, uint32_t W, uint64_t n, uint32_t* idx, float* val,
+                               uint64_t capacity, unsigned long long* counts, void* workspace, cudaStream_t s);
+cudaError_t launch_sparse_sum(const uint32_t* idx, const float* val, const unsigned long long* counts, uint32_t W,
+                              uint64_t capacity, uint64_t n, float* out, cudaStream_t s);
+
 // Library-owned scratch of s2_decode_compact_noalloc (see s2_decode.cu).
 uint64_t noalloc_compact_max_n();
 cudaError_t noalloc_compact_scratch(uint32_t** counts, uint32_t** offsets);
