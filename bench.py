@@ -579,6 +579,12 @@ def run_allgather(args, wl, world, rank, local):
                           "algorithmic_bytes_per_step": alg},
         "message_bytes_per_worker": {"allgather_lists": bytes_ag, "s2_sketch_and_bitmap": bytes_s2,
                                      "ratio_s2_over_allgather": round(bytes_s2 / max(bytes_ag, 1), 4)},
+        # bytes one worker receives in a ring collective over W workers: the
+        # AllGather brings every other worker's list, the AllReduce of the
+        # sketch and bitmap 2(W-1)/W of the message (reduce-scatter + gather)
+        "ring_bytes_received_per_worker": {
+            "allgather": (W - 1) * 8 * sum(nnz) // W,
+            "s2_allreduce": 2 * (W - 1) * bytes_s2 // W},
         "s2_decode_rel_l2_error_vs_exact": err,
         "gpu_launches": K * (2 + W + 1 + W),
         "clocks": clk.summary(),
