@@ -591,6 +591,65 @@ def run_allgather(args, wl, world, rank, local):
     }
 
 
+def encode_path_points():
+    """Workloads of the encode-path comparison: 8 workers of 2^22 uniform
+    positions with d = 3 and few buckets per row (16 .. 16384) at 1, 10 and
+    50 % density, where the L2 reductions of many nonzeros pile up on few
+    buckets; and the sweep points whose sketch fits in shared memory."""
+    pts = []
+    for w in (16, 64, 256, 1024, 4096, 16384):
+        for rho in (0.01, 0.1, 0.5):
+            pts.append(("custom", dict(W=8, n=1 << 22, d=3, w=w, density=rho, tag=7)))
+    for e in (20, 22, 24):
+        for dt in ("f32", "bf16"):
+            for d in (3, 5):
+                p = dict(n=1 << e, dtype=dt, density=0.001, d=d)
+                if 4 * d * workloads.sweep_w(int(round(0.001 * (1 << e)))) <= 192 * 1024:
+                    pts.append(("sweep", p))
+    return pts
+
+
+def run_encode_paths(args):
+    """Encode alone (s2_encode_batched_path) on each point with the L2 path,
+    the shared-memory path and the automatic choice; median of the timed
+    repetitions, L2 flushed before each."""
+    import torch
+
+    import sketch_compressed_sparse_gb300 as s2
+
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    reps = max(5, min(args.steps, 30))
+    rows = []
+    with ClockSampler(physical_gpu_index(0)) as clk:
+        for kind, p in encode_path_points():
+            wl = workloads.custom(**p) if kind == "custom" else workloads.sweep_point(**p)
+            g = wl.dense_torch(dev)
+            W, n = g.shape
+            bm, sk = s2.alloc_encode_outputs(W, n, wl.d, wl.w, dev)
+            row = {"workload": wl.name, "W": W, "n": n, "d": wl.d, "w": wl.w, "density": p["density"],
+                   "dtype": wl.dtype}
+            for path in ("l2", "smem", "auto"):
+                for _ in range(max(3, args.warmup)):
+                    s2.s2_encode_batched_path(g, wl.d, wl.w, wl.seed, bm, sk, path=path)
+                ts = []
+                for r in range(reps):
+                    flush.fill_(float(r & 7))
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    s2.s2_encode_batched_path(g, wl.d, wl.w, wl.seed, bm, sk, path=path)
+                    b.record()
+                    torch.cuda.synchronize(dev)
+                    ts.append(a.elapsed_time(b))
+                row[path + "_ms"] = round(statistics.median(ts), 5)
+            row["smem_speedup"] = round(row["l2_ms"] / row["smem_ms"], 3)
+            rows.append(row)
+            del g, bm, sk
+    return {"metric": "encode ms per step, L2 vs shared-memory sketch path", "unit": "ms", "n_gpus": 1,
+            "repetitions": reps, "data": "synthetic", "l2": "flushed before every repetition (512 MiB write)",
+            "points": rows, "clocks": clk.summary()}
+
+
 def run_e2e(args, wl, dev, s2):
     """Host pinned grad -> device -> path -> host out, through s2_pipeline_dense_host."""
     import torch
@@ -698,9 +757,19 @@ def main(argv=None):
                     help="profiling aid: keep only the first K workers of the workload (changes the workload)")
     ap.add_argument("--ceilings", action="store_true",
                     help="build and run ceilings.cu (device ceilings of scattered L2 operations) and exit")
+    ap.add_argument("--encode-paths", action="store_true",
+                    help="time encode on the L2 and the shared-memory sketch paths over small-sketch workloads, "
+                         "print one JSON line and exit")
     args = ap.parse_args(argv)
     if args.ceilings:
         return run_ceilings(args)
+    if args.encode_paths:
+        res = run_encode_paths(args)
+        print(json.dumps(res), flush=True)
+        if args.out:
+            with open(args.out, "a") as f:
+                f.write(json.dumps(res) + "\n")
+        return 0
     if args.warmup < 3 and args.impl == "ours" and args.steps > 5:
         ap.error("use at least 3 warm-up steps")
 

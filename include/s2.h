@@ -106,6 +106,36 @@ S2_API s2_status s2_encode(const void *grad, s2_dtype dt, uint64_t n, s2_params 
 S2_API s2_status s2_encode_batched(const void *grad, s2_dtype dt, uint32_t W, uint64_t n, s2_params p,
                             uint32_t *bitmaps, float *sketches, s2_stream_t stream);
 
+/* Where the count-sketch inserts of an encode accumulate. */
+typedef enum {
+    S2_PATH_AUTO = 0, /* the library picks one of the two below */
+    S2_PATH_L2 = 1,   /* float reductions straight into the sketch in global memory (resolved in L2) */
+    S2_PATH_SMEM = 2  /* a private copy of the sketch per thread block in shared memory, added into the
+                         global sketch once at the end; only for 4*d*w <= S2_SMEM_SKETCH_MAX_BYTES */
+} s2_encode_path;
+
+#define S2_SMEM_SKETCH_MAX_BYTES (192u * 1024u)
+
+/*
+ * s2_encode_batched_path -- s2_encode_batched with the accumulation path
+ * chosen by the caller (s2_encode_batched is this call with S2_PATH_AUTO).
+ * The results are the same on both paths up to the order of the float32
+ * adds: identical bitmaps, sketches within float32 rounding of each other.
+ * S2_PATH_SMEM: each thread block owns a contiguous range of one worker's
+ * positions and adds its inserts into a d x w copy in shared memory (lanes of
+ * a warp that hit the same bucket in one step are merged first), then adds
+ * the copy into the worker's sketch (stores it when one block covers the
+ * worker). A sketch larger than S2_SMEM_SKETCH_MAX_BYTES returns
+ * S2_ERR_UNSUPPORTED. S2_PATH_AUTO takes the shared-memory path when the
+ * sketch fits, n >= 4096*w (many positions per bucket, so that the adds of a
+ * moderately dense gradient pile up on each bucket) and the blocks' final
+ * additions cost at most half as many L2 sector operations as reading the
+ * gradient; otherwise the L2 path.
+ */
+S2_API s2_status s2_encode_batched_path(const void *grad, s2_dtype dt, uint32_t W, uint64_t n, s2_params p,
+                                        s2_encode_path path, uint32_t *bitmaps, float *sketches,
+                                        s2_stream_t stream);
+
 /*
  * s2_encode_batched_blocks -- s2_encode_batched with the paper's block-granular
  * bitmap (Section 3.1 "Compressing Sparse Gradient": one bit per word vector

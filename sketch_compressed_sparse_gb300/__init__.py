@@ -24,6 +24,11 @@ __all__ = [
     "nwords",
     "s2_encode",
     "s2_encode_batched",
+    "s2_encode_batched_path",
+    "S2_PATH_AUTO",
+    "S2_PATH_L2",
+    "S2_PATH_SMEM",
+    "S2_SMEM_SKETCH_MAX_BYTES",
     "s2_reduce",
     "s2_encode_reduce_fused",
     "s2_encode_batched_blocks",
@@ -63,6 +68,7 @@ _u32, _u64, _i32, _f32, _vp, _sz = (ctypes.c_uint32, ctypes.c_uint64, ctypes.c_i
 _SIGS = {
     "s2_encode": ([_vp, _i32, _u64, Params, _vp, _vp, _vp], _i32),
     "s2_encode_batched": ([_vp, _i32, _u32, _u64, Params, _vp, _vp, _vp], _i32),
+    "s2_encode_batched_path": ([_vp, _i32, _u32, _u64, Params, _i32, _vp, _vp, _vp], _i32),
     "s2_reduce": ([_vp, _vp, _u32, _u64, Params, _vp, _vp, _vp], _i32),
     "s2_encode_reduce_fused": ([_vp, _i32, _u32, _u64, Params, _vp, _vp, _vp], _i32),
     "s2_encode_batched_blocks": ([_vp, _i32, _u32, _u64, _u32, Params, _vp, _vp, _vp], _i32),
@@ -188,6 +194,26 @@ def s2_encode_batched(grad: torch.Tensor, d: int, w: int, seed: int, bitmaps: to
     _check(_f("s2_encode_batched")(_dev(grad, "grad", _GRAD), _dtype_code(grad), W, n, Params(d, w, seed),
                  _dev(bitmaps, "bitmaps", _U32, W * nwords(n)),
                  _dev(sketches, "sketches", (torch.float32,), W * d * w), _stream(stream)), "s2_encode_batched")
+
+
+S2_PATH_AUTO, S2_PATH_L2, S2_PATH_SMEM = 0, 1, 2
+S2_SMEM_SKETCH_MAX_BYTES = 192 * 1024
+_PATHS = {"auto": S2_PATH_AUTO, "l2": S2_PATH_L2, "smem": S2_PATH_SMEM}
+
+
+def s2_encode_batched_path(grad: torch.Tensor, d: int, w: int, seed: int, bitmaps: torch.Tensor,
+                           sketches: torch.Tensor, path="auto", stream=None) -> None:
+    """s2_encode_batched with the accumulation path: "auto", "l2" or "smem"
+    (a per-block copy of the sketch in shared memory; 4*d*w must be at most
+    S2_SMEM_SKETCH_MAX_BYTES)."""
+    if grad.dim() != 2:
+        raise ValueError("grad must be [W, n]")
+    code = _PATHS[path] if isinstance(path, str) else int(path)
+    W, n = grad.shape
+    _check(_f("s2_encode_batched_path")(_dev(grad, "grad", _GRAD), _dtype_code(grad), W, n, Params(d, w, seed),
+                                        code, _dev(bitmaps, "bitmaps", _U32, W * nwords(n)),
+                                        _dev(sketches, "sketches", (torch.float32,), W * d * w), _stream(stream)),
+           "s2_encode_batched_path")
 
 
 def s2_reduce(bitmaps: torch.Tensor, sketches: torch.Tensor, n: int, d: int, w: int, bitmap_out: torch.Tensor,

@@ -29,6 +29,35 @@ cudaError_t device_info(DeviceInfo* out) {
     return cudaSuccess;
 }
 
+int blocks_per_sm(const void* fn, int threads, size_t smem) {
+    struct Entry {
+        int dev;
+        const void* fn;
+        int threads;
+        size_t smem;
+        int per_sm;
+    };
+    static std::mutex mu;
+    static Entry table[512];
+    static int used = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int x = 0; x < used; ++x)
+            if (table[x].dev == dev && table[x].fn == fn && table[x].threads == threads && table[x].smem == smem)
+                return table[x].per_sm;
+    }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem) != cudaSuccess || per_sm < 1) {
+        cudaGetLastError();  // a failed query is not a launch error
+        return 1;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (used < 512) table[used++] = Entry{dev, fn, threads, smem, per_sm};
+    return per_sm;
+}
+
 static uint32_t host_fmix32(uint32_t x) {
     x ^= x >> 16;
     x *= 0x85ebca6bu;
@@ -56,6 +85,7 @@ using namespace s2;
 namespace {
 
 constexpr uint64_t kMaxN = 0xffffffffull;  // positions are 32-bit
+static_assert(kPrivMaxBytes == S2_SMEM_SKETCH_MAX_BYTES, "shared-memory sketch limit differs from the header");
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -82,7 +112,8 @@ inline size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 // whose sketches fit in half of L2 together, so that each group's
 // sketches are zeroed, updated and written back once.
 s2_status encode_impl(const void* grad, s2_dtype dt, uint32_t W, uint64_t n, s2_params p, uint32_t* bitmaps,
-                      float* sketches, cudaStream_t stream, uint32_t block = 0) {
+                      float* sketches, cudaStream_t stream, uint32_t block = 0,
+                      s2_encode_path path = S2_PATH_AUTO) {
     const uint64_t esz = dt == S2_F32 ? 4 : 2;
     const uint64_t nw = words_of(n);
     const uint64_t dw = (uint64_t)p.d * p.w;
@@ -110,6 +141,16 @@ s2_status encode_impl(const void* grad, s2_dtype dt, uint32_t W, uint64_t n, s2_
     if (block && W * nbw) {  // block bits are set with atomicOr: start from zero
         e = launch_zero(reinterpret_cast<float*>(bitmaps), W * nbw, stream);
         if (e != cudaSuccess) return S2_ERR_CUDA;
+    }
+    if (path != S2_PATH_L2 && sk_bytes <= kPrivMaxBytes) {
+        a.grad = grad;
+        a.bitmaps = bitmaps;
+        a.sketches = sketches;
+        a.workers = W;
+        bool launched = false;
+        e = launch_encode_smem(a, dt == S2_F32 ? 0 : 1, vec, path == S2_PATH_AUTO, &launched, stream);
+        if (e != cudaSuccess) return S2_ERR_CUDA;
+        if (launched) return S2_OK;
     }
     for (uint64_t k0 = 0; k0 < W; k0 += group) {
         const uint64_t g = (W - k0) < group ? (W - k0) : group;
@@ -228,6 +269,16 @@ s2_status s2_encode_batched(const void* grad, s2_dtype dt, uint32_t W, uint64_t 
     s2_status st = check_encode(grad, dt, W, n, p, bitmaps, sketches);
     if (st != S2_OK || W == 0) return st;
     return encode_impl(grad, dt, W, n, p, bitmaps, sketches, reinterpret_cast<cudaStream_t>(stream));
+}
+
+s2_status s2_encode_batched_path(const void* grad, s2_dtype dt, uint32_t W, uint64_t n, s2_params p,
+                                 s2_encode_path path, uint32_t* bitmaps, float* sketches, s2_stream_t stream) {
+    if (path != S2_PATH_AUTO && path != S2_PATH_L2 && path != S2_PATH_SMEM) return S2_ERR_INVALID_ARG;
+    s2_status st = check_encode(grad, dt, W, n, p, bitmaps, sketches);
+    if (st != S2_OK) return st;
+    if (path == S2_PATH_SMEM && (uint64_t)p.d * p.w * 4 > S2_SMEM_SKETCH_MAX_BYTES) return S2_ERR_UNSUPPORTED;
+    if (W == 0) return S2_OK;
+    return encode_impl(grad, dt, W, n, p, bitmaps, sketches, reinterpret_cast<cudaStream_t>(stream), 0, path);
 }
 
 s2_status s2_encode_batched_blocks(const void* grad, s2_dtype dt, uint32_t W, uint64_t n, uint32_t block,

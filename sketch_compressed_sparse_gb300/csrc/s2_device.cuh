@@ -80,6 +80,12 @@ __device__ __forceinline__ void red_add_f32(float* p, float v) {
     asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
+// Four float reductions into 16 consecutive bytes (p 16-byte aligned).
+__device__ __forceinline__ void red_add_f32x4(float* p, float4 v) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
 // L2 eviction-priority policies (createpolicy); "last" keeps a line in L2
 // ahead of normal and evict-first lines, "first" lets a line go first.
 __device__ __forceinline__ uint64_t policy_evict_last() {

@@ -359,6 +359,224 @@ __global__ void __launch_bounds__(kThreads) encode_scalar(EncodeArgs a) {
     }
 }
 
+// ---- shared-memory privatised sketch ----------------------------------------
+// For a sketch small enough to live in shared memory (4*d*w at most
+// kPrivMaxBytes), each block owns a contiguous range of one worker's tasks
+// and accumulates that range's inserts in a private d x w copy in shared
+// memory; lanes of a warp that hit the same bucket in the same step are
+// merged first (AGG), so each shared-memory atomic carries one bucket's sum.
+// At the end the copy is added into the worker's sketch in global memory
+// with d*w/4 vector reductions (or stored, when one block covers the whole
+// worker): the L2 sees d*w/4 operations per block instead of d per nonzero.
+//
+// The task registers of every load layout fit in four 16-byte vectors:
+//   L = 0: fp32, vector loads: slot 4u+c is position u*128 + 4*lane + c;
+//   L = 1: bf16, vector loads: slot 8u+c is position u*256 + 8*lane + c;
+//   L = 2: fp32, 4-byte loads: slot u is position u*32 + lane;
+//   L = 3: bf16, 2-byte loads: as L = 2, the value in the word's upper half.
+constexpr int kPrivThreads = 1024;
+
+template <int L>
+__device__ __forceinline__ void load_task(uint4 (&v)[4], const void* row, uint64_t e0, uint64_t n, int lane) {
+    if constexpr (L == 0) {
+        load_f32_task(v, static_cast<const float*>(row), e0, n, lane);
+    } else if constexpr (L == 1) {
+        const uint16_t* g = static_cast<const uint16_t*>(row);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const uint64_t e = e0 + u * 256 + lane * 8;
+            if (e + 8 <= n) {
+                v[u] = ld_stream_u4(g + e);
+            } else {
+                uint32_t h[4] = {0, 0, 0, 0};
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    if (e + c < n) h[c >> 1] |= (uint32_t)ld_stream_u16(g + e + c) << (16 * (c & 1));
+                v[u] = make_uint4(h[0], h[1], h[2], h[3]);
+            }
+        }
+        v[2] = v[3] = make_uint4(0, 0, 0, 0);
+    } else {
+        uint32_t x[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const uint64_t e = e0 + u * 32 + lane;
+            x[u] = 0;
+            if (e < n) {
+                if constexpr (L == 2)
+                    x[u] = ld_stream_u32(static_cast<const float*>(row) + e);
+                else
+                    x[u] = (uint32_t)ld_stream_u16(static_cast<const uint16_t*>(row) + e) << 16;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = make_uint4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
+    }
+}
+
+// Nonzero mask of the lane's 16 slots; *word gets bitmap word `lane` of the
+// task (meaningful on lanes 0..15).
+template <int L>
+__device__ __forceinline__ uint32_t task_bits(const uint4 (&v)[4], int lane, uint32_t* word) {
+    uint32_t mask = 0, my_word = 0;
+    if constexpr (L == 0) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t nib = ((v[u].x & 0x7fffffffu) != 0) | (((v[u].y & 0x7fffffffu) != 0) << 1) |
+                                 (((v[u].z & 0x7fffffffu) != 0) << 2) | (((v[u].w & 0x7fffffffu) != 0) << 3);
+            mask |= nib << (4 * u);
+            uint32_t part = nib << (4 * (lane & 7));
+            part |= __shfl_xor_sync(kFull, part, 1);
+            part |= __shfl_xor_sync(kFull, part, 2);
+            part |= __shfl_xor_sync(kFull, part, 4);
+            const uint32_t got = __shfl_sync(kFull, part, (lane & 3) * 8);
+            if ((lane >> 2) == u) my_word = got;
+        }
+    } else if constexpr (L == 1) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const uint32_t q[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+            uint32_t byte = 0;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                byte |= ((q[c] & 0x7fffu) != 0) << (2 * c);
+                byte |= ((q[c] & 0x7fff0000u) != 0) << (2 * c + 1);
+            }
+            mask |= byte << (8 * u);
+            uint32_t part = byte << (8 * (lane & 3));
+            part |= __shfl_xor_sync(kFull, part, 1);
+            part |= __shfl_xor_sync(kFull, part, 2);
+            const uint32_t got = __shfl_sync(kFull, part, (lane & 7) * 4);
+            if ((lane >> 3) == u) my_word = got;
+        }
+    } else {
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const uint4 q = v[u >> 2];
+            const uint32_t x = (u & 3) == 0 ? q.x : ((u & 3) == 1 ? q.y : ((u & 3) == 2 ? q.z : q.w));
+            const bool nz = (x & 0x7fffffffu) != 0;
+            const uint32_t b = __ballot_sync(kFull, nz);
+            mask |= (uint32_t)nz << u;
+            if (lane == u) my_word = b;
+        }
+    }
+    *word = my_word;
+    return mask;
+}
+
+template <int L>
+__device__ __forceinline__ uint32_t slot_bits(const uint4 (&v)[4], int slot) {
+    if constexpr (L == 1) {
+        const uint4 q = (slot < 8) ? v[0] : v[1];
+        const int c = slot & 7;
+        const uint32_t word = (c >> 1) == 0 ? q.x : ((c >> 1) == 1 ? q.y : ((c >> 1) == 2 ? q.z : q.w));
+        return (c & 1) ? (word & 0xffff0000u) : (word << 16);
+    } else {
+        return pick16(v, slot);
+    }
+}
+
+template <int L>
+__device__ __forceinline__ uint32_t slot_position(uint64_t e0, int slot, int lane) {
+    if constexpr (L == 0) return (uint32_t)(e0 + (slot >> 2) * 128 + lane * 4 + (slot & 3));
+    if constexpr (L == 1) return (uint32_t)(e0 + (slot >> 3) * 256 + lane * 8 + (slot & 7));
+    return (uint32_t)(e0 + slot * 32 + lane);
+}
+
+// Add v into tile[x] for every lane with act set; lanes with the same x are
+// merged first: the lowest of them adds the group's sum, taken in ascending
+// lane order. Called by all 32 lanes.
+__device__ __forceinline__ void smem_add_merged(float* tile, uint32_t x, float v, bool act, int lane) {
+    const uint32_t key = act ? x : 0xffffffffu;
+    const unsigned grp = __match_any_sync(kFull, key);
+    const int leader = __ffs(grp) - 1;
+    unsigned others = grp & (grp - 1);  // the group without its lowest lane
+    const int extra = (act && lane == leader) ? __popc(others) : 0;
+    const int rounds = __reduce_max_sync(kFull, (unsigned)extra);
+    float s = v;
+    for (int r = 0; r < rounds; ++r) {
+        const int src = others ? __ffs(others) - 1 : lane;
+        const float o = __shfl_sync(kFull, v, src);
+        if (others) {
+            s += o;
+            others &= others - 1;
+        }
+    }
+    if (act && lane == leader) atomicAdd(tile + x, s);
+}
+
+template <int D, int L, bool BLK, bool AGG>
+__global__ void __launch_bounds__(kPrivThreads) encode_priv(EncodeArgs a, uint32_t per_worker, int store) {
+    extern __shared__ __align__(16) float s_tile[];  // [d][w]
+    __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
+    const uint32_t dw = (uint32_t)a.dw;
+    for (uint32_t x = threadIdx.x; x < dw; x += blockDim.x) s_tile[x] = 0.f;
+    load_keys(a.keys, s_kh, s_ks);  // ends with __syncthreads
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const uint32_t k = blockIdx.x / per_worker, part = blockIdx.x - k * per_worker;
+    const uint64_t T = a.tasks_per_worker;
+    const uint64_t t1 = T * (part + 1) / per_worker;
+    constexpr uint64_t esz = (L == 1 || L == 3) ? 2 : 4;
+    const void* row = static_cast<const char*>(a.grad) + (uint64_t)k * a.n * esz;
+    const int rows = D > 0 ? D : a.d;
+    uint64_t t = T * part / per_worker + warp;
+    uint4 v[4];
+    if (t < t1) load_task<L>(v, row, t * kTaskElems, a.n, lane);
+    for (; t < t1; t += nwarps) {
+        const uint64_t e0 = t * kTaskElems;
+        const bool more = t + nwarps < t1;
+        uint4 nv[4];
+        if (more) load_task<L>(nv, row, (t + nwarps) * kTaskElems, a.n, lane);
+        uint32_t my_word;
+        uint32_t mask = task_bits<L>(v, lane, &my_word);
+        const uint64_t wi = t * kTaskWords + lane;
+        store_bitmap_word<BLK>(a, k, wi, my_word, lane < kTaskWords && wi < a.nw, lane);
+        while (__any_sync(kFull, mask != 0)) {
+            const bool act = mask != 0;
+            const int slot = act ? __ffs(mask) - 1 : 0;
+            mask &= mask - 1;
+            const uint32_t i = slot_position<L>(e0, slot, lane);
+            const float val = __uint_as_float(slot_bits<L>(v, slot));
+#pragma unroll
+            for (int j = 0; j < (D > 0 ? D : kMaxRows); ++j) {
+                if (D > 0 || j < rows) {
+                    const uint32_t x = (uint32_t)j * a.w + bucket_of(i, s_kh[j], a.w);
+                    const float sv = apply_sign(val, signbit_of(i, s_ks[j]));
+                    if (AGG)
+                        smem_add_merged(s_tile, x, sv, act, lane);
+                    else if (act)
+                        atomicAdd(s_tile + x, sv);
+                }
+            }
+        }
+        if (more) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = nv[u];
+        }
+    }
+    __syncthreads();
+    float* sk = a.sketches + (uint64_t)k * a.dw;
+    if ((dw & 3u) == 0) {  // every worker's sketch starts on a 16-byte boundary
+        const float4* t4 = reinterpret_cast<const float4*>(s_tile);
+        for (uint32_t x = threadIdx.x; x < dw / 4; x += blockDim.x) {
+            const float4 q = t4[x];
+            if (store)
+                reinterpret_cast<float4*>(sk)[x] = q;
+            else if (q.x != 0.f || q.y != 0.f || q.z != 0.f || q.w != 0.f)
+                red_add_f32x4(sk + 4 * x, q);
+        }
+    } else {
+        for (uint32_t x = threadIdx.x; x < dw; x += blockDim.x) {
+            const float q = s_tile[x];
+            if (store)
+                sk[x] = q;
+            else if (q != 0.f)
+                red_add_f32(sk + x, q);
+        }
+    }
+}
+
 // ---- 16-byte aligned rows: per-warp bulk-copy (TMA) pipeline -------------
 // Each warp owns a ring of kBulkStages shared-memory stages of 2 KB. Lane 0
 // keeps the warp's next tasks in flight with cp.async.bulk copies that
@@ -602,6 +820,98 @@ cudaError_t launch_encode_db(const EncodeArgs& a, int dtype, bool vec, cudaStrea
     return cudaGetLastError();
 }
 
+// ---- shared-memory path: planning and launch ------------------------------
+// Buckets per row up to which lanes hitting the same bucket are merged
+// before the shared-memory atomic. Measured on GB300 (8 workers of 2^22
+// positions, d = 3): merging pays only in rows of about 16 buckets with half
+// of the positions nonzero; from 64 buckets up, the match/shuffle work costs
+// more than the serialised same-address atomics it saves (up to 2.3x slower).
+constexpr uint32_t kAggMaxW = 16;
+
+template <int D, int L, bool BLK, bool AGG>
+cudaError_t launch_priv_t(const EncodeArgs& a, bool only_if_preferred, bool* launched, cudaStream_t s) {
+    auto kern = encode_priv<D, L, BLK, AGG>;
+    const size_t smem = (size_t)a.dw * 4;
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrivMaxBytes);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    DeviceInfo di{};
+    e = device_info(&di);
+    if (e != cudaSuccess) return e;
+    const int per_sm = blocks_per_sm(reinterpret_cast<const void*>(kern), kPrivThreads, smem);
+    // blocks per worker: enough to fill every SM, at most one per warp's task
+    const uint64_t slots = (uint64_t)di.sms * (uint64_t)(per_sm > 0 ? per_sm : 1);
+    uint64_t per_worker = (slots + a.workers - 1) / a.workers;
+    const uint64_t most = ((uint64_t)a.tasks_per_worker + kPrivThreads / 32 - 1) / (kPrivThreads / 32);
+    if (per_worker > most) per_worker = most;
+    if (per_worker < 1) per_worker = 1;
+    if (only_if_preferred) {
+        // Taken when a row has few buckets for the positions (at least 4096
+        // positions per bucket: from about 1% density on, every bucket takes
+        // tens of adds, which serialise in L2 but not in shared memory) and
+        // the blocks' final additions (d*w/4 operations each) cost at most
+        // half the sectors of the worker's gradient row (n*esz/32). Measured
+        // on GB300: 1.1x slower than the L2 path at 1% density, 2.5-20x
+        // faster at 10-50%; with the paper's sketch sizing (w about half the
+        // nonzeros, so fewer than 2000 positions per bucket) the L2 path,
+        // 5-15% faster there, is kept.
+        const uint64_t esz = (L == 1 || L == 3) ? 2 : 4;
+        if (a.n < (uint64_t)a.w * 4096 || per_worker * a.dw * 16 > a.n * esz) {
+            *launched = false;
+            return cudaSuccess;
+        }
+    }
+    if (per_worker > 1) {
+        e = launch_zero(a.sketches, (uint64_t)a.workers * a.dw, s);
+        if (e != cudaSuccess) return e;
+    }
+    const uint64_t esz = (L == 1 || L == 3) ? 2 : 4;
+    const uint64_t chunk = 0x7fffffffull / per_worker;  // workers per launch: grid below 2^31 blocks
+    for (uint64_t k0 = 0; k0 < a.workers; k0 += chunk) {
+        EncodeArgs b = a;
+        b.workers = (uint32_t)((a.workers - k0) < chunk ? (a.workers - k0) : chunk);
+        b.grad = static_cast<const char*>(a.grad) + k0 * a.n * esz;
+        b.bitmaps = a.bitmaps + k0 * (BLK ? a.nbw : a.nw);
+        b.sketches = a.sketches + k0 * a.dw;
+        kern<<<(unsigned)(b.workers * per_worker), kPrivThreads, smem, s>>>(b, (uint32_t)per_worker,
+                                                                          per_worker == 1 ? 1 : 0);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    *launched = true;
+    return cudaSuccess;
+}
+
+template <int D, int L, bool BLK>
+cudaError_t launch_priv_l(const EncodeArgs& a, bool only_if_preferred, bool* launched, cudaStream_t s) {
+    return a.w <= kAggMaxW ? launch_priv_t<D, L, BLK, true>(a, only_if_preferred, launched, s)
+                           : launch_priv_t<D, L, BLK, false>(a, only_if_preferred, launched, s);
+}
+
+template <int D, bool BLK>
+cudaError_t launch_priv_db(const EncodeArgs& a, int dtype, bool vec, bool only_if_preferred, bool* launched,
+                           cudaStream_t s) {
+    if (vec) {
+        return dtype == 0 ? launch_priv_l<D, 0, BLK>(a, only_if_preferred, launched, s)
+                          : launch_priv_l<D, 1, BLK>(a, only_if_preferred, launched, s);
+    }
+    return dtype == 0 ? launch_priv_l<D, 2, BLK>(a, only_if_preferred, launched, s)
+                      : launch_priv_l<D, 3, BLK>(a, only_if_preferred, launched, s);
+}
+
+template <int D>
+cudaError_t launch_priv_d(const EncodeArgs& a, int dtype, bool vec, bool only_if_preferred, bool* launched,
+                          cudaStream_t s) {
+    return a.block_words ? launch_priv_db<D, true>(a, dtype, vec, only_if_preferred, launched, s)
+                         : launch_priv_db<D, false>(a, dtype, vec, only_if_preferred, launched, s);
+}
+
 template <int D>
 cudaError_t launch_encode_d(const EncodeArgs& a, int dtype, bool vec, cudaStream_t s) {
     return a.block_words ? launch_encode_db<D, true>(a, dtype, vec, s) : launch_encode_db<D, false>(a, dtype, vec, s);
@@ -616,6 +926,21 @@ cudaError_t launch_encode(const EncodeArgs& a, int dtype, bool vec, cudaStream_t
         case 5: return launch_encode_d<5>(a, dtype, vec, s);
         case 1: return launch_encode_d<1>(a, dtype, vec, s);
         default: return launch_encode_d<0>(a, dtype, vec, s);
+    }
+}
+
+cudaError_t launch_encode_smem(const EncodeArgs& a, int dtype, bool vec, bool only_if_preferred, bool* launched,
+                               cudaStream_t s) {
+    *launched = false;
+    if ((uint64_t)a.dw * 4 > kPrivMaxBytes) return cudaSuccess;
+    if (a.workers == 0 || a.tasks_per_worker == 0) {  // nothing to read: the sketches are zero
+        *launched = true;
+        return launch_zero(a.sketches, (uint64_t)a.workers * a.dw, s);
+    }
+    switch (a.d) {
+        case 3: return launch_priv_d<3>(a, dtype, vec, only_if_preferred, launched, s);
+        case 5: return launch_priv_d<5>(a, dtype, vec, only_if_preferred, launched, s);
+        default: return launch_priv_d<0>(a, dtype, vec, only_if_preferred, launched, s);
     }
 }
 

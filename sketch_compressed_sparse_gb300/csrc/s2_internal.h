@@ -44,6 +44,14 @@ struct EncodeArgs {
 // dtype: 0 = f32, 1 = bf16. vec: rows are 16-byte aligned (vector loads).
 cudaError_t launch_encode(const EncodeArgs& a, int dtype, bool vec, cudaStream_t s);
 cudaError_t launch_zero(float* p, uint64_t count, cudaStream_t s);
+
+// Shared-memory privatised sketches (4*d*w <= kPrivMaxBytes), all a.workers
+// workers in one pass; zeroes the sketches itself when it needs to. With
+// only_if_preferred the launch is skipped (*launched = false) when the
+// blocks' final additions would cost more than half of the gradient read.
+constexpr size_t kPrivMaxBytes = 192 * 1024;
+cudaError_t launch_encode_smem(const EncodeArgs& a, int dtype, bool vec, bool only_if_preferred, bool* launched,
+                               cudaStream_t s);
 cudaError_t take_encode_fault(unsigned int* out);
 
 // ---- fused encode + reduce (single sketch) ----------------------------------
@@ -109,20 +117,15 @@ cudaError_t noalloc_compact_scratch(uint32_t** counts, uint32_t** offsets);
 cudaError_t launch_hash(const uint32_t* idx, uint64_t m, uint32_t d, uint32_t w, RowKeys keys,
                         uint32_t* bucket_out, int8_t* sign_out, cudaStream_t s);
 
+// Resident blocks per SM of kernel `fn` (occupancy calculator, cached per
+// device, kernel, block size and dynamic shared memory); at least 1.
+int blocks_per_sm(const void* fn, int threads, size_t smem);
+
 // Blocks to launch for a grid-stride kernel: a multiple of the SM count
 // (resident blocks per SM from the occupancy calculator), capped by the work.
 template <typename Kernel>
 int grid_for(Kernel k, uint64_t work_blocks, size_t smem = 0) {
-    static int cached[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-    int per_sm = cached[dev];
-    if (per_sm == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, smem) != cudaSuccess ||
-            per_sm < 1)
-            per_sm = 1;
-        cached[dev] = per_sm;
-    }
+    const int per_sm = blocks_per_sm(reinterpret_cast<const void*>(k), kThreads, smem);
     DeviceInfo di{};
     if (device_info(&di) != cudaSuccess) di.sms = 1;
     uint64_t full = (uint64_t)di.sms * (uint64_t)per_sm;
