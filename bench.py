@@ -255,6 +255,28 @@ def time_oracle(wl: workloads.Workload, G: np.ndarray, reps: int) -> dict:
     return {"seconds": t, "reps": reps, "value": wl.W * wl.n / t / 1e9}
 
 
+def time_oracle_threads(wl: workloads.Workload, G: np.ndarray) -> dict:
+    """The oracle's steps as they stand, with the W workers' encodes on W
+    host threads at once (each call runs in C outside the interpreter lock);
+    reduce and decode on one thread."""
+    import concurrent.futures as cf
+
+    import oracle
+
+    oracle.build()
+    threads = max(1, min(wl.W, os.cpu_count() or 1))
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        parts = list(ex.map(lambda k: oracle.encode(G[k], wl.d, wl.w, wl.seed, wl.dtype), range(wl.W)))
+    bms = np.stack([p[0] for p in parts])
+    S = np.stack([p[1] for p in parts])
+    A = np.stack([p[2] for p in parts])
+    bm, Ssum, Asum = oracle.reduce(bms, S, A)
+    oracle.decode_dense(bm, Ssum, wl.n, wl.seed, 1.0, Asum)
+    t = time.perf_counter() - t0
+    return {"seconds": t, "threads": threads, "value": wl.W * wl.n / t / 1e9}
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args, wl, world, rank, local):
@@ -426,6 +448,11 @@ def run_ours(args, wl, world, rank, local):
         res["cpu_baseline"] = {"value": round(o["value"], 5), "unit": "Gelem/s", "cores": 1, "kind": "oracle",
                                "sample": f"one full encode->reduce->decode of this workload on the host "
                                          f"({o['seconds']:.2f} s, single thread, plain C, fp64)"}
+        ot = time_oracle_threads(wl, G)
+        res["cpu_baseline_threads"] = {
+            "value": round(ot["value"], 5), "unit": "Gelem/s", "cores": ot["threads"], "kind": "oracle",
+            "sample": f"the same pass with the {wl.W} workers' encodes on {ot['threads']} host threads, reduce and "
+                      f"decode on one ({ot['seconds']:.2f} s; host has {os.cpu_count()} cores)"}
     return res
 
 
@@ -650,6 +677,42 @@ def run_encode_paths(args):
             "points": rows, "clocks": clk.summary()}
 
 
+def run_sweep(args):
+    """The sweep grid (8 workers, n = 2^20 .. 2^max, fp32/bf16, density 0.1 /
+    1 / 10 %, d = 3 or 5, w = nnz/2 rounded to a power of two) through the
+    per-worker path, one compact row per point."""
+    import copy
+
+    import torch
+
+    rows = []
+    sub = copy.copy(args)
+    sub.no_e2e, sub.no_cpu, sub.block, sub.mode = True, True, 0, "per_worker"
+    sub.steps = max(5, min(args.steps, 30))
+    sub.warmup = max(3, args.warmup)
+    t0 = time.perf_counter()
+    for p in workloads.sweep_grid():
+        if p["n"] > (1 << args.sweep_max_log2):
+            continue
+        wl = workloads.sweep_point(**p)
+        r = run_ours(sub, wl, 1, 0, 0)
+        rows.append({"n": wl.n, "dtype": wl.dtype, "density": p["density"], "d": wl.d, "w": wl.w,
+                     "nnz_union": r["config"]["nnz_union"], "ms_per_step": r["ms_per_step"],
+                     "gelem_s": r["value"], "stages_ms": r["stages_ms_per_step"],
+                     "hbm_frac_path": r["path_roofline"]["frac"],
+                     "l2_frac": r["l2_roofline"].get("frac")})
+        del wl
+        torch.cuda.empty_cache()
+    peaks = measured_peaks()
+    return {"metric": METRIC + " (sweep grid)", "unit": "Gelem/s", "n_gpus": 1, "steps_per_point": sub.steps,
+            "warmup": sub.warmup, "higher_is_better": True, "data": "synthetic",
+            "config": {"workload": "sweep: W=8, n=2^20..2^%d, fp32/bf16, density 0.1/1/10 %%, d in {3,5}, "
+                                   "w = 2^round(log2(nnz/2))" % args.sweep_max_log2,
+                       "l2": "flushed before every step (512 MiB write)"},
+            "hbm_peak_gbs": peaks["hbm_gbs"], "points": rows,
+            "wall_s": round(time.perf_counter() - t0, 1)}
+
+
 def run_e2e(args, wl, dev, s2):
     """Host pinned grad -> device -> path -> host out, through s2_pipeline_dense_host."""
     import torch
@@ -743,7 +806,10 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="embedding", choices=["tiny", "embedding", "topk", "large_lm", "blocktopk"])
+    ap.add_argument("--config", default="embedding",
+                    choices=["tiny", "embedding", "topk", "large_lm", "blocktopk", "sweep"])
+    ap.add_argument("--sweep-max-log2", type=int, default=28,
+                    help="--config sweep: largest gradient length as a power of two (20..28)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle timing")
     ap.add_argument("--e2e-steps", type=int, default=20)
@@ -777,7 +843,7 @@ def main(argv=None):
     if args.impl == "reference":
         if rank != 0:
             return 0
-        if args.config == "blocktopk":
+        if args.config in ("blocktopk", "sweep"):
             res = {"impl": "reference", "unavailable": "the CPU reference arm covers the four S2 workloads only"}
         else:
             res = run_reference(args, workloads.by_name(args.config))
@@ -790,6 +856,8 @@ def main(argv=None):
             dist.init_process_group("nccl")
         if args.config == "blocktopk":
             res = run_blocktopk(args, world, rank, local)
+        elif args.config == "sweep":
+            res = run_sweep(args)
         elif args.mode == "allgather":
             res = run_allgather(args, workloads.by_name(args.config), world, rank, local)
         else:

@@ -92,8 +92,13 @@ class Workload:
         return g
 
     def union_nnz(self) -> int:
-        u = np.unique(np.concatenate(self.idx)) if self.W else np.zeros(0)
-        return int(u.size)
+        """Positions that are nonzero in at least one worker."""
+        if not self.W:
+            return 0
+        mark = np.zeros(self.n, dtype=bool)
+        for ix in self.idx:
+            mark[ix] = True
+        return int(np.count_nonzero(mark))
 
     def describe(self) -> dict:
         return {
