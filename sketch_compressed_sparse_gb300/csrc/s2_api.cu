@@ -124,6 +124,16 @@ s2_status encode_impl(const void* grad, s2_dtype dt, uint32_t W, uint64_t n, s2_
     uint64_t group = sk_bytes ? ((uint64_t)di.l2_bytes / 2) / sk_bytes : W;
     if (group < 1) group = 1;
     if (group > W) group = W;
+    // A sketch too large to stay in L2 while it is built (above 70% of L2:
+    // its reductions would go to DRAM) is built one worker at a time in
+    // `passes` slices of its flattened buckets, each pass re-reading the
+    // worker's gradient and updating only its slice.
+    const uint64_t slice_cap = (uint64_t)di.l2_bytes / 10 * 7;
+    uint64_t passes = 1;
+    if (sk_bytes > slice_cap && path != S2_PATH_SMEM) {
+        passes = (sk_bytes + slice_cap - 1) / slice_cap;
+        group = 1;
+    }
     // vector loads need every worker row 16-byte aligned
     const bool vec = ((n * esz) % 16 == 0) || W == 1;
     EncodeArgs a;
@@ -138,6 +148,8 @@ s2_status encode_impl(const void* grad, s2_dtype dt, uint32_t W, uint64_t n, s2_
     const uint64_t nbw = block ? words_of((n + block - 1) / block) : 0;
     a.block_words = block / 32;
     a.nbw = nbw;
+    a.x_lo = 0;
+    a.x_span = dw;
     if (block && W * nbw) {  // block bits are set with atomicOr: start from zero
         e = launch_zero(reinterpret_cast<float*>(bitmaps), W * nbw, stream);
         if (e != cudaSuccess) return S2_ERR_CUDA;
@@ -154,14 +166,30 @@ s2_status encode_impl(const void* grad, s2_dtype dt, uint32_t W, uint64_t n, s2_
     }
     for (uint64_t k0 = 0; k0 < W; k0 += group) {
         const uint64_t g = (W - k0) < group ? (W - k0) : group;
-        e = launch_zero(sketches + k0 * dw, g * dw, stream);
-        if (e != cudaSuccess) return S2_ERR_CUDA;
         a.grad = static_cast<const char*>(grad) + k0 * n * esz;
         a.bitmaps = bitmaps + k0 * (block ? nbw : nw);
         a.sketches = sketches + k0 * dw;
         a.workers = (uint32_t)g;
-        e = launch_encode(a, dt == S2_F32 ? 0 : 1, vec, stream);
-        if (e != cudaSuccess) return S2_ERR_CUDA;
+        if (passes == 1) {
+            e = launch_zero(sketches + k0 * dw, g * dw, stream);
+            if (e != cudaSuccess) return S2_ERR_CUDA;
+            e = launch_encode(a, dt == S2_F32 ? 0 : 1, vec, stream);
+            if (e != cudaSuccess) return S2_ERR_CUDA;
+            continue;
+        }
+        // one worker, slice by slice (the bitmap is rewritten with the same
+        // words on every pass; block bits are ORed again)
+        const uint64_t span = (dw + passes - 1) / passes;
+        for (uint64_t x0 = 0; x0 < dw; x0 += span) {
+            a.x_lo = x0;
+            a.x_span = (dw - x0) < span ? (dw - x0) : span;
+            e = launch_zero(sketches + k0 * dw + x0, a.x_span, stream);
+            if (e != cudaSuccess) return S2_ERR_CUDA;
+            e = launch_encode(a, dt == S2_F32 ? 0 : 1, vec, stream);
+            if (e != cudaSuccess) return S2_ERR_CUDA;
+        }
+        a.x_lo = 0;
+        a.x_span = dw;
     }
     return S2_OK;
 }

@@ -26,17 +26,21 @@ __device__ __forceinline__ uint32_t pick16(const uint4 (&v)[4], int slot) {
 
 // Insert value `val` of position `i` into every row of the sketch. The
 // reductions carry an evict-last L2 policy: the sketch being built must stay
-// in L2 while the gradient streams past it.
+// in L2 while the gradient streams past it. Only buckets whose flattened
+// index j*w + b lies in the launch's slice [a.x_lo, a.x_lo + a.x_span) are
+// updated (a sketch larger than L2 is built one slice per pass).
 template <int D>
-__device__ __forceinline__ void insert(float* __restrict__ sk, uint32_t i, float val, int d, uint32_t w,
+__device__ __forceinline__ void insert(float* __restrict__ sk, uint32_t i, float val, const EncodeArgs& a,
                                        const uint32_t* s_kh, const uint32_t* s_ks, uint64_t keep) {
-    const int rows = D > 0 ? D : d;
+    const int rows = D > 0 ? D : a.d;
 #pragma unroll
     for (int j = 0; j < (D > 0 ? D : kMaxRows); ++j) {
         if (D > 0 || j < rows) {
-            uint32_t b = bucket_of(i, s_kh[j], w);
-            uint32_t sb = signbit_of(i, s_ks[j]);
-            red_add_f32_hint(sk + (uint64_t)j * w + b, apply_sign(val, sb), keep);
+            const uint64_t x = (uint64_t)j * a.w + bucket_of(i, s_kh[j], a.w);
+            if (x - a.x_lo < a.x_span) {
+                const uint32_t sb = signbit_of(i, s_ks[j]);
+                red_add_f32_hint(sk + x, apply_sign(val, sb), keep);
+            }
         }
     }
 }
@@ -102,9 +106,9 @@ constexpr uint32_t kDenseTask = 32;  // a task with at least this many nonzeros 
 
 template <int D>
 __device__ __forceinline__ void insert_listed(const uint32_t* lpos, const float* lval, uint32_t cnt, int lane,
-                                              float* sk, int d, uint32_t w, const uint32_t* s_kh,
+                                              float* sk, const EncodeArgs& a, const uint32_t* s_kh,
                                               const uint32_t* s_ks, uint64_t keep) {
-    if ((uint32_t)lane < cnt) insert<D>(sk, lpos[lane], lval[lane], d, w, s_kh, s_ks, keep);
+    if ((uint32_t)lane < cnt) insert<D>(sk, lpos[lane], lval[lane], a, s_kh, s_ks, keep);
 }
 
 // fp32 rows, 16-byte aligned. Dense tasks (>= kDenseTask nonzeros, e.g. the
@@ -172,12 +176,11 @@ __global__ void __launch_bounds__(kThreads) encode_f32_vec(EncodeArgs a) {
                 const int slot = __ffs(mask) - 1;
                 mask &= mask - 1;
                 const uint32_t i = (uint32_t)(e0 + (slot >> 2) * 128 + lane * 4 + (slot & 3));
-                insert<D>(sk, i, __uint_as_float(pick16(v, slot)), a.d, a.w, s_kh, s_ks, keep);
+                insert<D>(sk, i, __uint_as_float(pick16(v, slot)), a, s_kh, s_ks, keep);
             }
         } else if (total > 0) {
             if (k != lk && lcount > 0) {  // the list belongs to another worker: drain it first
-                insert_listed<D>(lpos, lval, lcount, lane, a.sketches + (uint64_t)lk * a.dw, a.d, a.w, s_kh, s_ks,
-                                 keep);
+                insert_listed<D>(lpos, lval, lcount, lane, a.sketches + (uint64_t)lk * a.dw, a, s_kh, s_ks, keep);
                 __syncwarp();
                 lcount = 0;
             }
@@ -191,7 +194,7 @@ __global__ void __launch_bounds__(kThreads) encode_f32_vec(EncodeArgs a) {
             lcount += total;  // at most 31 + 31 < kListCap
             __syncwarp();
             if (lcount >= 32) {
-                insert_listed<D>(lpos, lval, 32, lane, a.sketches + (uint64_t)lk * a.dw, a.d, a.w, s_kh, s_ks, keep);
+                insert_listed<D>(lpos, lval, 32, lane, a.sketches + (uint64_t)lk * a.dw, a, s_kh, s_ks, keep);
                 const uint32_t rest = lcount - 32;
                 uint32_t p = 0;
                 float q = 0.f;
@@ -218,7 +221,7 @@ __global__ void __launch_bounds__(kThreads) encode_f32_vec(EncodeArgs a) {
         }
     }
     if (lcount > 0)
-        insert_listed<D>(lpos, lval, lcount, lane, a.sketches + (uint64_t)lk * a.dw, a.d, a.w, s_kh, s_ks, keep);
+        insert_listed<D>(lpos, lval, lcount, lane, a.sketches + (uint64_t)lk * a.dw, a, s_kh, s_ks, keep);
 }
 
 // ---- bf16, 16-byte vector loads --------------------------------------------
@@ -286,7 +289,7 @@ __global__ void __launch_bounds__(kThreads) encode_bf16_vec(EncodeArgs a) {
             const uint32_t word = (c >> 1) == 0 ? q.x : ((c >> 1) == 1 ? q.y : ((c >> 1) == 2 ? q.z : q.w));
             const uint32_t bits = (c & 1) ? (word & 0xffff0000u) : (word << 16);
             const uint32_t i = (uint32_t)(e0 + (slot >> 3) * 256 + lane * 8 + c);
-            insert<D>(sk, i, __uint_as_float(bits), a.d, a.w, s_kh, s_ks, keep);
+            insert<D>(sk, i, __uint_as_float(bits), a, s_kh, s_ks, keep);
         }
         local += nwarps;
         while (local >= a.tasks_per_worker && k < a.workers) {
@@ -349,7 +352,7 @@ __global__ void __launch_bounds__(kThreads) encode_scalar(EncodeArgs a) {
 #pragma unroll
             for (int s = 1; s < 16; ++s) bits = (slot == s) ? x[s] : bits;
             const uint32_t i = (uint32_t)(e0 + slot * 32 + lane);
-            insert<D>(sk, i, __uint_as_float(bits), a.d, a.w, s_kh, s_ks, keep);
+            insert<D>(sk, i, __uint_as_float(bits), a, s_kh, s_ks, keep);
         }
         local += nwarps;
         while (local >= a.tasks_per_worker && k < a.workers) {
@@ -741,16 +744,7 @@ __global__ void __launch_bounds__(kThreads) encode_bulk(EncodeArgs a) {
             const uint32_t p = list[r];
             const uint32_t bits = BF16 ? (uint32_t)(*reinterpret_cast<const uint16_t*>(st + 2 * p)) << 16
                                        : *reinterpret_cast<const uint32_t*>(st + 4 * p);
-            const float val = __uint_as_float(bits);
-            const uint32_t i = (uint32_t)(e0 + p);
-            const int rows = D > 0 ? D : a.d;
-#pragma unroll
-            for (int j = 0; j < (D > 0 ? D : kMaxRows); ++j) {
-                if (D > 0 || j < rows) {
-                    const uint32_t b = bucket_of(i, s_kh[j], a.w);
-                    red_add_f32_hint(sk + (uint64_t)j * a.w + b, apply_sign(val, signbit_of(i, s_ks[j])), keep);
-                }
-            }
+            insert<D>(sk, (uint32_t)(e0 + p), __uint_as_float(bits), a, s_kh, s_ks, keep);
         }
         // Every lane has consumed its reads of this stage and of the list
         // (their values fed the reductions), so both may be overwritten.

@@ -39,6 +39,8 @@ struct EncodeArgs {
     RowKeys keys;
     uint32_t block_words;  // 0: element bitmap; else one bit per block of this many bitmap words
     uint64_t nbw;          // block bitmap words per worker (block mode)
+    uint64_t x_lo;         // slice of the flattened sketch (j*w + b) this launch updates:
+    uint64_t x_span;       //   [x_lo, x_lo + x_span); [0, d*w) in a single pass
 };
 
 // dtype: 0 = f32, 1 = bf16. vec: rows are 16-byte aligned (vector loads).
