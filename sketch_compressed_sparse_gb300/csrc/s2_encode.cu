@@ -26,10 +26,10 @@ __device__ __forceinline__ uint32_t pick16(const uint4 (&v)[4], int slot) {
 
 // Insert value `val` of position `i` into every row of the sketch. The
 // reductions carry an evict-last L2 policy: the sketch being built must stay
-// in L2 while the gradient streams past it. Only buckets whose flattened
+// in L2 while the gradient streams past it. SL: only buckets whose flattened
 // index j*w + b lies in the launch's slice [a.x_lo, a.x_lo + a.x_span) are
 // updated (a sketch larger than L2 is built one slice per pass).
-template <int D>
+template <int D, bool SL>
 __device__ __forceinline__ void insert(float* __restrict__ sk, uint32_t i, float val, const EncodeArgs& a,
                                        const uint32_t* s_kh, const uint32_t* s_ks, uint64_t keep) {
     const int rows = D > 0 ? D : a.d;
@@ -37,7 +37,7 @@ __device__ __forceinline__ void insert(float* __restrict__ sk, uint32_t i, float
     for (int j = 0; j < (D > 0 ? D : kMaxRows); ++j) {
         if (D > 0 || j < rows) {
             const uint64_t x = (uint64_t)j * a.w + bucket_of(i, s_kh[j], a.w);
-            if (x - a.x_lo < a.x_span) {
+            if (!SL || x - a.x_lo < a.x_span) {
                 const uint32_t sb = signbit_of(i, s_ks[j]);
                 red_add_f32_hint(sk + x, apply_sign(val, sb), keep);
             }
@@ -104,11 +104,11 @@ __device__ __forceinline__ void load_f32_task(uint4 (&v)[4], const float* g, uin
 constexpr uint32_t kListCap = 64;
 constexpr uint32_t kDenseTask = 32;  // a task with at least this many nonzeros is walked per lane
 
-template <int D>
+template <int D, bool SL>
 __device__ __forceinline__ void insert_listed(const uint32_t* lpos, const float* lval, uint32_t cnt, int lane,
                                               float* sk, const EncodeArgs& a, const uint32_t* s_kh,
                                               const uint32_t* s_ks, uint64_t keep) {
-    if ((uint32_t)lane < cnt) insert<D>(sk, lpos[lane], lval[lane], a, s_kh, s_ks, keep);
+    if ((uint32_t)lane < cnt) insert<D, SL>(sk, lpos[lane], lval[lane], a, s_kh, s_ks, keep);
 }
 
 // fp32 rows, 16-byte aligned. Dense tasks (>= kDenseTask nonzeros, e.g. the
@@ -118,7 +118,7 @@ __device__ __forceinline__ void insert_listed(const uint32_t* lpos, const float*
 // at a time with every lane busy, so their d reductions do not run on lone
 // lanes. The list only holds one worker's entries; it is drained when the
 // warp moves on to another worker and at the end.
-template <int D, bool BLK>
+template <int D, bool BLK, bool SL>
 __global__ void __launch_bounds__(kThreads) encode_f32_vec(EncodeArgs a) {
     __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
     __shared__ uint32_t s_lpos[kThreads / 32][kListCap];
@@ -176,11 +176,11 @@ __global__ void __launch_bounds__(kThreads) encode_f32_vec(EncodeArgs a) {
                 const int slot = __ffs(mask) - 1;
                 mask &= mask - 1;
                 const uint32_t i = (uint32_t)(e0 + (slot >> 2) * 128 + lane * 4 + (slot & 3));
-                insert<D>(sk, i, __uint_as_float(pick16(v, slot)), a, s_kh, s_ks, keep);
+                insert<D, SL>(sk, i, __uint_as_float(pick16(v, slot)), a, s_kh, s_ks, keep);
             }
         } else if (total > 0) {
             if (k != lk && lcount > 0) {  // the list belongs to another worker: drain it first
-                insert_listed<D>(lpos, lval, lcount, lane, a.sketches + (uint64_t)lk * a.dw, a, s_kh, s_ks, keep);
+                insert_listed<D, SL>(lpos, lval, lcount, lane, a.sketches + (uint64_t)lk * a.dw, a, s_kh, s_ks, keep);
                 __syncwarp();
                 lcount = 0;
             }
@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kThreads) encode_f32_vec(EncodeArgs a) {
             lcount += total;  // at most 31 + 31 < kListCap
             __syncwarp();
             if (lcount >= 32) {
-                insert_listed<D>(lpos, lval, 32, lane, a.sketches + (uint64_t)lk * a.dw, a, s_kh, s_ks, keep);
+                insert_listed<D, SL>(lpos, lval, 32, lane, a.sketches + (uint64_t)lk * a.dw, a, s_kh, s_ks, keep);
                 const uint32_t rest = lcount - 32;
                 uint32_t p = 0;
                 float q = 0.f;
@@ -221,14 +221,14 @@ __global__ void __launch_bounds__(kThreads) encode_f32_vec(EncodeArgs a) {
         }
     }
     if (lcount > 0)
-        insert_listed<D>(lpos, lval, lcount, lane, a.sketches + (uint64_t)lk * a.dw, a, s_kh, s_ks, keep);
+        insert_listed<D, SL>(lpos, lval, lcount, lane, a.sketches + (uint64_t)lk * a.dw, a, s_kh, s_ks, keep);
 }
 
 // ---- bf16, 16-byte vector loads --------------------------------------------
 // Lane l loads positions u*256 + 8l .. +7 for u = 0..1; slot 8u + c is
 // position u*256 + 8l + c. Word q of chunk u is made of the bytes of lanes
 // 4q .. 4q+3.
-template <int D, bool BLK>
+template <int D, bool BLK, bool SL>
 __global__ void __launch_bounds__(kThreads) encode_bf16_vec(EncodeArgs a) {
     __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
     load_keys(a.keys, s_kh, s_ks);
@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(kThreads) encode_bf16_vec(EncodeArgs a) {
             const uint32_t word = (c >> 1) == 0 ? q.x : ((c >> 1) == 1 ? q.y : ((c >> 1) == 2 ? q.z : q.w));
             const uint32_t bits = (c & 1) ? (word & 0xffff0000u) : (word << 16);
             const uint32_t i = (uint32_t)(e0 + (slot >> 3) * 256 + lane * 8 + c);
-            insert<D>(sk, i, __uint_as_float(bits), a, s_kh, s_ks, keep);
+            insert<D, SL>(sk, i, __uint_as_float(bits), a, s_kh, s_ks, keep);
         }
         local += nwarps;
         while (local >= a.tasks_per_worker && k < a.workers) {
@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(kThreads) encode_bf16_vec(EncodeArgs a) {
 // ---- any alignment: one element per lane and load -------------------------
 // Lane l loads position u*32 + l for u = 0..15; a ballot gives word u
 // directly; slot u is position u*32 + l.
-template <int D, bool BF16, bool BLK>
+template <int D, bool BF16, bool BLK, bool SL>
 __global__ void __launch_bounds__(kThreads) encode_scalar(EncodeArgs a) {
     __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
     load_keys(a.keys, s_kh, s_ks);
@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(kThreads) encode_scalar(EncodeArgs a) {
 #pragma unroll
             for (int s = 1; s < 16; ++s) bits = (slot == s) ? x[s] : bits;
             const uint32_t i = (uint32_t)(e0 + slot * 32 + lane);
-            insert<D>(sk, i, __uint_as_float(bits), a, s_kh, s_ks, keep);
+            insert<D, SL>(sk, i, __uint_as_float(bits), a, s_kh, s_ks, keep);
         }
         local += nwarps;
         while (local >= a.tasks_per_worker && k < a.workers) {
@@ -744,7 +744,7 @@ __global__ void __launch_bounds__(kThreads) encode_bulk(EncodeArgs a) {
             const uint32_t p = list[r];
             const uint32_t bits = BF16 ? (uint32_t)(*reinterpret_cast<const uint16_t*>(st + 2 * p)) << 16
                                        : *reinterpret_cast<const uint32_t*>(st + 4 * p);
-            insert<D>(sk, (uint32_t)(e0 + p), __uint_as_float(bits), a, s_kh, s_ks, keep);
+            insert<D, false>(sk, (uint32_t)(e0 + p), __uint_as_float(bits), a, s_kh, s_ks, keep);
         }
         // Every lane has consumed its reads of this stage and of the list
         // (their values fed the reductions), so both may be overwritten.
@@ -790,28 +790,35 @@ cudaError_t launch_bulk(const EncodeArgs& a, uint64_t tasks, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <int D, bool BLK>
-cudaError_t launch_encode_db(const EncodeArgs& a, int dtype, bool vec, cudaStream_t s) {
+template <int D, bool BLK, bool SL>
+cudaError_t launch_encode_dbs(const EncodeArgs& a, int dtype, bool vec, cudaStream_t s) {
     const uint64_t tasks = (uint64_t)a.workers * a.tasks_per_worker;
     const uint64_t blocks = (tasks + (kThreads / 32) - 1) / (kThreads / 32);
     const uint64_t esz = dtype == 0 ? 4 : 2;
     const bool rows_aligned = (a.n * esz) % 16 == 0;
-    if (!BLK && kUseBulk && vec && rows_aligned) {
+    if (!BLK && !SL && kUseBulk && vec && rows_aligned) {
         EncodeArgs b = a;  // bulk tasks are 2 KB of gradient
         b.tasks_per_worker = (uint32_t)((a.n * esz + kBulkTaskBytes - 1) / kBulkTaskBytes);
         const uint64_t btasks = (uint64_t)b.workers * b.tasks_per_worker;
         return dtype == 0 ? launch_bulk<D, false>(b, btasks, s) : launch_bulk<D, true>(b, btasks, s);
     }
     if (vec && dtype == 0) {
-        encode_f32_vec<D, BLK><<<grid_for(encode_f32_vec<D, BLK>, blocks), kThreads, 0, s>>>(a);
+        encode_f32_vec<D, BLK, SL><<<grid_for(encode_f32_vec<D, BLK, SL>, blocks), kThreads, 0, s>>>(a);
     } else if (vec && dtype == 1) {
-        encode_bf16_vec<D, BLK><<<grid_for(encode_bf16_vec<D, BLK>, blocks), kThreads, 0, s>>>(a);
+        encode_bf16_vec<D, BLK, SL><<<grid_for(encode_bf16_vec<D, BLK, SL>, blocks), kThreads, 0, s>>>(a);
     } else if (dtype == 0) {
-        encode_scalar<D, false, BLK><<<grid_for(encode_scalar<D, false, BLK>, blocks), kThreads, 0, s>>>(a);
+        encode_scalar<D, false, BLK, SL><<<grid_for(encode_scalar<D, false, BLK, SL>, blocks), kThreads, 0, s>>>(a);
     } else {
-        encode_scalar<D, true, BLK><<<grid_for(encode_scalar<D, true, BLK>, blocks), kThreads, 0, s>>>(a);
+        encode_scalar<D, true, BLK, SL><<<grid_for(encode_scalar<D, true, BLK, SL>, blocks), kThreads, 0, s>>>(a);
     }
     return cudaGetLastError();
+}
+
+// Slices (x_span < d*w) are only used with the element bitmap.
+template <int D, bool BLK>
+cudaError_t launch_encode_db(const EncodeArgs& a, int dtype, bool vec, cudaStream_t s) {
+    if (!BLK && a.x_span < a.dw) return launch_encode_dbs<D, false, true>(a, dtype, vec, s);
+    return launch_encode_dbs<D, BLK, false>(a, dtype, vec, s);
 }
 
 // ---- shared-memory path: planning and launch ------------------------------
