@@ -740,7 +740,9 @@ def run_e2e(args, wl, dev, s2):
         t += a.elapsed_time(b) / 1e3
     return {"value": round(wl.W * wl.n * K / t / 1e9, 3), "unit": "Gelem/s",
             "h2d_bytes_per_step": int(wl.W * wl.n * wl.elem_bytes), "d2h_bytes_per_step": int(4 * wl.n),
-            "steps": K, "ms_per_step": round(t / K * 1e3, 4)}
+            "steps": K, "ms_per_step": round(t / K * 1e3, 4),
+            "transfer": "pinned host gradient and output; the library's kernels read and write them in place "
+                        "(mapped page-locked memory), so the host<->device bytes move inside the kernels"}
 
 
 # ---------------------------------------------------------------- reference arm (the oracle)

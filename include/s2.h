@@ -313,10 +313,16 @@ S2_API s2_status s2_pipeline_workspace_size(s2_dtype dt, uint32_t W, uint64_t n,
 
 /*
  * s2_pipeline_dense_host -- the whole path from HOST memory to HOST memory:
- * copy grad [W][n] to the device, s2_encode_batched, s2_reduce,
- * s2_decode_dense, and copy the decoded [n] float32 vector back.
- *   host_grad / host_out: host memory; pinned (page-locked) memory makes the
- *   copies asynchronous, pageable memory makes them synchronous.
+ * grad [W][n] to the device, s2_encode_batched, s2_reduce, s2_decode_dense,
+ * and the decoded [n] float32 vector back to the host.
+ *   host_grad / host_out: host memory. Page-locked memory that the device can
+ *   address (cudaHostAlloc, cudaHostRegister, torch pin_memory), 16-byte
+ *   aligned, is accessed in place by the kernels: the encode reads the
+ *   gradient from it and the decode writes the output to it, with no copy
+ *   (the gradient is still staged when the sketch is larger than 3/4 of the
+ *   L2 cache, where the encode reads it more than once). Other host memory
+ *   is staged through the workspace with copies, which are synchronous for
+ *   pageable memory.
  *   workspace: device scratch of s2_pipeline_workspace_size bytes, 16-byte
  *   aligned. The call returns once the work is queued on `stream`; host_out
  *   is valid after the stream is synchronised.

@@ -367,7 +367,8 @@ def s2_pipeline_workspace_size(dtype: torch.dtype, W: int, n: int, d: int, w: in
 
 def s2_pipeline_dense_host(host_grad: torch.Tensor, d: int, w: int, seed: int, host_out: torch.Tensor,
                            workspace: torch.Tensor, scale: float = 1.0, stream=None) -> None:
-    """HOST grad [W, n] (pinned for async copies) -> HOST out [n]; queued on the stream."""
+    """HOST grad [W, n] -> HOST out [n]; queued on the stream. Pinned tensors
+    are read / written in place by the kernels; pageable ones are staged."""
     if host_grad.is_cuda or host_out.is_cuda:
         raise ValueError("s2_pipeline_dense_host takes host tensors")
     if host_grad.dim() != 2 or host_grad.dtype not in _GRAD or not host_grad.is_contiguous():

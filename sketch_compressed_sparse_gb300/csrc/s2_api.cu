@@ -260,6 +260,19 @@ DecodeArgs make_decode_args(const uint32_t* bitmap, const float* sketch, uint64_
     return a;
 }
 
+// Device address of page-locked host memory at `p` that the current device
+// can access in place (16-byte aligned), or nullptr for any other memory.
+const void* mapped_host(const void* p) {
+    if (!p) return nullptr;
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();  // an unknown pointer is not an error here
+        return nullptr;
+    }
+    if (at.type != cudaMemoryTypeHost || !at.devicePointer || !aligned(at.devicePointer, 16)) return nullptr;
+    return at.devicePointer;
+}
+
 struct PipelineLayout {
     size_t grad, bitmaps, sketches, bitmap, sketch, out, total;
 };
@@ -586,19 +599,37 @@ s2_status s2_pipeline_dense_host(const void* host_grad, s2_dtype dt, uint32_t W,
     uint32_t* d_bitmap = reinterpret_cast<uint32_t*>(ws + L.bitmap);
     float* d_sketch = reinterpret_cast<float*>(ws + L.sketch);
     float* d_out = reinterpret_cast<float*>(ws + L.out);
-    if ((uint64_t)W * n > 0 &&
-        cudaMemcpyAsync(d_grad, host_grad, (size_t)W * n * esz, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return S2_ERR_CUDA;
-    if (W > 0) {
-        st = encode_impl(d_grad, dt, W, n, p, d_bitmaps, d_sketches, s);
+    // Page-locked host buffers mapped into the device's address space are
+    // read and written in place by the kernels (over NVLink-C2C on a
+    // Grace-Blackwell node): the encode streams the gradient from host
+    // memory once and the decode stores the output there, so no staging
+    // copy precedes or follows them. Other host memory is staged through
+    // the workspace with copies. A sketch built in several passes (larger
+    // than 3/4 of L2) would re-read the gradient per pass: staged too.
+    const void* enc_src = d_grad;
+    if ((uint64_t)W * n > 0) {
+        DeviceInfo di{};
+        if (device_info(&di) != cudaSuccess) return S2_ERR_CUDA;
+        const bool one_pass = (uint64_t)p.d * p.w * 4 <= (uint64_t)di.l2_bytes / 4 * 3;
+        const void* mapped = one_pass ? mapped_host(host_grad) : nullptr;
+        if (mapped) {
+            enc_src = mapped;
+        } else if (cudaMemcpyAsync(d_grad, host_grad, (size_t)W * n * esz, cudaMemcpyHostToDevice, s) !=
+                   cudaSuccess) {
+            return S2_ERR_CUDA;
+        }
+        st = encode_impl(enc_src, dt, W, n, p, d_bitmaps, d_sketches, s);
         if (st != S2_OK) return st;
     }
     st = s2_reduce(d_bitmaps, d_sketches, W, n, p, d_bitmap, d_sketch, stream);
     if (st != S2_OK) return st;
     if (n == 0) return S2_OK;
-    st = s2_decode_dense(d_bitmap, d_sketch, n, p, scale, d_out, stream);
+    float* out_mapped = static_cast<float*>(const_cast<void*>(mapped_host(host_out)));
+    st = s2_decode_dense(d_bitmap, d_sketch, n, p, scale, out_mapped ? out_mapped : d_out, stream);
     if (st != S2_OK) return st;
-    if (cudaMemcpyAsync(host_out, d_out, (size_t)n * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess) return S2_ERR_CUDA;
+    if (!out_mapped &&
+        cudaMemcpyAsync(host_out, d_out, (size_t)n * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return S2_ERR_CUDA;
     return S2_OK;
 }
 

@@ -261,6 +261,39 @@ def test_pipeline_dense_host_matches_oracle():
     assert_decoded_close(ho.numpy(), ref["out"], ref["amax"])
 
 
+@pytest.mark.parametrize("pin_in,pin_out", [(False, False), (True, False), (False, True)])
+def test_pipeline_dense_host_staged_and_in_place(pin_in, pin_out):
+    # pinned buffers are read / written in place by the kernels, pageable
+    # ones are staged with copies: the results must be the same
+    wl = workloads.custom(W=3, n=40_000, d=3, w=1024, density=0.05, dtype="bf16", tag=1101)
+    G = wl.dense()
+    hg = torch.from_numpy(G.view(np.int16)).view(torch.bfloat16)
+    hg = hg.pin_memory() if pin_in else hg.clone()
+    ho = torch.full((wl.n,), 3.0, dtype=torch.float32)
+    ho = ho.pin_memory() if pin_out else ho
+    ws = torch.empty(s2.s2_pipeline_workspace_size(torch.bfloat16, wl.W, wl.n, wl.d, wl.w), dtype=torch.uint8,
+                     device=DEV)
+    s2.s2_pipeline_dense_host(hg, wl.d, wl.w, wl.seed, ho, ws)
+    torch.cuda.synchronize()
+    ref = oracle.pipeline(G, wl.d, wl.w, wl.seed, dtype="bf16")
+    assert_decoded_close(ho.numpy(), ref["out"], ref["amax"])
+
+
+def test_pipeline_dense_host_unaligned_pinned_input_is_staged():
+    wl = workloads.custom(W=2, n=10_000, d=3, w=512, density=0.05, tag=1102)
+    G = wl.dense()
+    buf = torch.zeros(G.size + 1, dtype=torch.float32).pin_memory()
+    buf[1:] = torch.from_numpy(G.reshape(-1))
+    hg = buf[1:].view(wl.W, wl.n)  # 4 bytes past a pinned allocation: not 16-byte aligned
+    ho = torch.empty(wl.n, dtype=torch.float32).pin_memory()
+    ws = torch.empty(s2.s2_pipeline_workspace_size(torch.float32, wl.W, wl.n, wl.d, wl.w), dtype=torch.uint8,
+                     device=DEV)
+    s2.s2_pipeline_dense_host(hg, wl.d, wl.w, wl.seed, ho, ws)
+    torch.cuda.synchronize()
+    ref = oracle.pipeline(G, wl.d, wl.w, wl.seed)
+    assert_decoded_close(ho.numpy(), ref["out"], ref["amax"])
+
+
 def test_non_default_stream():
     wl = workloads.custom(W=3, n=30_000, d=3, w=1000, density=0.05, tag=1200)
     g = _grad(wl)
