@@ -648,8 +648,16 @@ def run_encode_paths(args):
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     reps = max(5, min(args.steps, 30))
     rows = []
+    want = {}
+    for kv in filter(None, (args.paths_select or "").split(",")):
+        k, v = kv.split("=")
+        want[k.strip()] = float(v)
     with ClockSampler(physical_gpu_index(0)) as clk:
         for kind, p in encode_path_points():
+            if kind != "custom" and want:
+                continue
+            if any(float(p.get(k, -1)) != v for k, v in want.items()):
+                continue
             wl = workloads.custom(**p) if kind == "custom" else workloads.sweep_point(**p)
             g = wl.dense_torch(dev)
             W, n = g.shape
@@ -825,6 +833,8 @@ def main(argv=None):
                     help="profiling aid: keep only the first K workers of the workload (changes the workload)")
     ap.add_argument("--ceilings", action="store_true",
                     help="build and run ceilings.cu (device ceilings of scattered L2 operations) and exit")
+    ap.add_argument("--paths-select", default=None,
+                    help="--encode-paths: keep only the small-sketch points matching e.g. 'w=256,density=0.5'")
     ap.add_argument("--encode-paths", action="store_true",
                     help="time encode on the L2 and the shared-memory sketch paths over small-sketch workloads, "
                          "print one JSON line and exit")
