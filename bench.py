@@ -115,10 +115,20 @@ def measured_ceilings():
         return json.load(f)
 
 
-def encode_launches(wl: workloads.Workload, l2_bytes: int) -> int:
+def encode_launches(wl: workloads.Workload, l2_bytes: int, sms: int = 152) -> int:
     """Kernels one s2_encode_batched call launches: a zero fill and an encode per
-    group of workers whose sketches fit in half of L2 together."""
+    group of workers whose sketches fit in half of L2 together; per worker and
+    slice when the sketch is built in passes (above 3/4 of L2); a zero fill and
+    one shared-memory encode when the library takes that path."""
     sk = 4 * wl.d * wl.w
+    esz = 4 if wl.dtype == "f32" else 2
+    tasks = (wl.n + 511) // 512
+    per_worker = max(1, min(-(-sms // max(wl.W, 1)), -(-tasks // 32)))
+    if sk <= 192 * 1024 and wl.n >= 4096 * wl.w and per_worker * wl.d * wl.w * 16 <= wl.n * esz:
+        return 2 if per_worker > 1 else 1
+    cap = l2_bytes // 4 * 3
+    if sk > cap:
+        return 2 * wl.W * (-(-sk // cap))
     group = max(1, min(wl.W, (l2_bytes // 2) // sk)) if sk else wl.W
     return 2 * ((wl.W + group - 1) // group)
 
