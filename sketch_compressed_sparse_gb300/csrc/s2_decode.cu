@@ -101,8 +101,14 @@ __device__ __forceinline__ uint32_t lane_mask_blocks(const DecodeArgs& a, uint64
     return mask;
 }
 
+// Tasks a launch handles: every task; only tasks without a set position
+// (their 512 zeros); only tasks with one. An output larger than L2 is written
+// in the two last phases, zeros first, so that the zero stream does not
+// evict the summed sketch while the gathers need it.
+enum DensePhase : int { kAllTasks = 0, kEmptyTasks = 1, kSetTasks = 2 };
+
 template <int D, bool BLK>
-__global__ void __launch_bounds__(kThreads) decode_dense_kernel(DecodeArgs a, float* __restrict__ out) {
+__global__ void __launch_bounds__(kThreads) decode_dense_kernel(DecodeArgs a, float* __restrict__ out, int phase) {
     __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
     load_keys(a.keys, s_kh, s_ks);
     const int lane = threadIdx.x & 31;
@@ -118,6 +124,10 @@ __global__ void __launch_bounds__(kThreads) decode_dense_kernel(DecodeArgs a, fl
         } else {
             const uint32_t my_word = lane < kTaskWords ? load_word(a.bitmap, wi, a.nw, a.n) : 0u;
             mask = lane_mask(my_word, lane);
+        }
+        if (phase != kAllTasks) {
+            const bool any = __any_sync(kFull, mask != 0);  // warp-uniform
+            if (any != (phase == kSetTasks)) continue;
         }
         float r[16];
 #pragma unroll
@@ -298,7 +308,18 @@ template <int D, bool BLK>
 cudaError_t launch_dense_db(const DecodeArgs& a, float* out, cudaStream_t s) {
     const uint64_t tasks = (a.n + kTaskElems - 1) / kTaskElems;
     const uint64_t blocks = (tasks + (kThreads / 32) - 1) / (kThreads / 32);
-    decode_dense_kernel<D, BLK><<<grid_for(decode_dense_kernel<D, BLK>, blocks), kThreads, 0, s>>>(a, out);
+    const int grid = grid_for(decode_dense_kernel<D, BLK>, blocks);
+    DeviceInfo di{};
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return e;
+    if (a.n * 4 <= (uint64_t)di.l2_bytes) {
+        decode_dense_kernel<D, BLK><<<grid, kThreads, 0, s>>>(a, out, kAllTasks);
+        return cudaGetLastError();
+    }
+    decode_dense_kernel<D, BLK><<<grid, kThreads, 0, s>>>(a, out, kEmptyTasks);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    decode_dense_kernel<D, BLK><<<grid, kThreads, 0, s>>>(a, out, kSetTasks);
     return cudaGetLastError();
 }
 

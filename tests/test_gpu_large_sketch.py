@@ -1,6 +1,7 @@
 """GPU parity for sketches larger than the L2 cache can hold while they are
 built (more than 3/4 of L2): the encode then builds each worker's sketch in
-several passes, each over one slice of the flattened buckets. The results
+several passes, each over one slice of the flattened buckets; and for dense
+outputs larger than L2, which the decode writes in two launches. The results
 must be those of the single-pass definition: bitmaps bit for bit, sketches
 and decoded values within the stated tolerance, and bit for bit on
 integer-valued gradients.
@@ -42,3 +43,12 @@ def test_ragged_slices_bf16_unaligned_rows():
 def test_multi_pass_exact_on_integers():
     run(workloads.custom(W=3, n=65_536, d=3, w=(1 << 24) + 1, density=0.1, values="int", int_max=256, tag=703),
         exact=True)
+
+
+def test_dense_output_larger_than_l2_is_written_in_two_phases():
+    # 4n bytes of output above the L2 size: tasks without a set position are
+    # written (zeros) by a first launch, the others by a second one
+    n = (l2_bytes() // 4) + 5_000_003
+    wl = workloads.custom(W=2, n=n, d=3, w=1 << 16, density=0.001, tag=704)
+    got = gpu_pipeline(wl.dense_torch("cuda"), wl.d, wl.w, wl.seed)
+    check_pipeline(wl.dense(), wl.dtype, got, wl.d, wl.w, wl.seed)
