@@ -333,11 +333,13 @@ S2_API s2_status s2_pipeline_dense_host(const void *host_grad, s2_dtype dt, uint
 
 /*
  * s2_take_device_fault -- read and clear this device's fault word.
- *   Kernels that wait on their own asynchronous copies bound every wait; if a
- *   wait ever gives up, the kernel records a nonzero code here and returns
- *   early, so the outputs of the calls since the last check are not valid.
- *   *fault_out receives the code (0 = no fault). Synchronises with the device
- *   (it reads device memory); call it between steps, not inside a hot loop.
+ *   A kernel that waits on its own asynchronous copies must bound every wait
+ *   and, if a wait gives up, record a nonzero code here and return early (the
+ *   outputs of the calls since the last check are then not valid). No kernel
+ *   of this version waits on anything, so the word stays 0; the call is kept
+ *   so that callers can check it between steps. *fault_out receives the code
+ *   (0 = no fault). Synchronises with the device (it reads device memory);
+ *   call it between steps, not inside a hot loop.
  */
 S2_API s2_status s2_take_device_fault(uint32_t *fault_out);
 

@@ -101,14 +101,14 @@ __device__ __forceinline__ uint32_t lane_mask_blocks(const DecodeArgs& a, uint64
     return mask;
 }
 
-// Tasks a launch handles: every task; only tasks without a set position
-// (their 512 zeros); only tasks with one. An output larger than L2 is written
-// in the two last phases, zeros first, so that the zero stream does not
-// evict the summed sketch while the gathers need it.
-enum DensePhase : int { kAllTasks = 0, kEmptyTasks = 1, kSetTasks = 2 };
-
-template <int D, bool BLK>
-__global__ void __launch_bounds__(kThreads) decode_dense_kernel(DecodeArgs a, float* __restrict__ out, int phase) {
+// PHASED: the launch handles only the tasks without a set position (their
+// 512 zeros; set_tasks = 0) or only the tasks with one (set_tasks = 1). An
+// output larger than L2 is written in these two launches, zeros first, so
+// that the zero stream does not evict the summed sketch while the gathers
+// need it. Without PHASED every task is handled (and the kernel carries no
+// phase test).
+template <int D, bool BLK, bool PHASED>
+__global__ void __launch_bounds__(kThreads) decode_dense_kernel(DecodeArgs a, float* __restrict__ out, int set_tasks) {
     __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
     load_keys(a.keys, s_kh, s_ks);
     const int lane = threadIdx.x & 31;
@@ -125,9 +125,9 @@ __global__ void __launch_bounds__(kThreads) decode_dense_kernel(DecodeArgs a, fl
             const uint32_t my_word = lane < kTaskWords ? load_word(a.bitmap, wi, a.nw, a.n) : 0u;
             mask = lane_mask(my_word, lane);
         }
-        if (phase != kAllTasks) {
+        if (PHASED) {
             const bool any = __any_sync(kFull, mask != 0);  // warp-uniform
-            if (any != (phase == kSetTasks)) continue;
+            if (any != (set_tasks != 0)) continue;
         }
         float r[16];
 #pragma unroll
@@ -308,18 +308,19 @@ template <int D, bool BLK>
 cudaError_t launch_dense_db(const DecodeArgs& a, float* out, cudaStream_t s) {
     const uint64_t tasks = (a.n + kTaskElems - 1) / kTaskElems;
     const uint64_t blocks = (tasks + (kThreads / 32) - 1) / (kThreads / 32);
-    const int grid = grid_for(decode_dense_kernel<D, BLK>, blocks);
     DeviceInfo di{};
     cudaError_t e = device_info(&di);
     if (e != cudaSuccess) return e;
     if (a.n * 4 <= (uint64_t)di.l2_bytes) {
-        decode_dense_kernel<D, BLK><<<grid, kThreads, 0, s>>>(a, out, kAllTasks);
+        decode_dense_kernel<D, BLK, false>
+            <<<grid_for(decode_dense_kernel<D, BLK, false>, blocks), kThreads, 0, s>>>(a, out, 0);
         return cudaGetLastError();
     }
-    decode_dense_kernel<D, BLK><<<grid, kThreads, 0, s>>>(a, out, kEmptyTasks);
+    const int grid = grid_for(decode_dense_kernel<D, BLK, true>, blocks);
+    decode_dense_kernel<D, BLK, true><<<grid, kThreads, 0, s>>>(a, out, 0);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    decode_dense_kernel<D, BLK><<<grid, kThreads, 0, s>>>(a, out, kSetTasks);
+    decode_dense_kernel<D, BLK, true><<<grid, kThreads, 0, s>>>(a, out, 1);
     return cudaGetLastError();
 }
 

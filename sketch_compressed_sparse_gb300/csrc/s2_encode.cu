@@ -12,6 +12,8 @@
 // Work is proportional to the nonzeros, whatever their pattern (whole rows or
 // scattered entries). Tasks are handed out worker-major so that the sketches
 // being written at any moment are those of one or two workers.
+#include <atomic>
+
 #include "s2_internal.h"
 
 namespace s2 {
@@ -45,12 +47,6 @@ __device__ __forceinline__ void insert(float* __restrict__ sk, uint32_t i, float
     }
 }
 
-// Tuning switches (compile-time): prefetch the next task's vectors into
-// registers before processing the current one; route 16-byte aligned rows
-// through the bulk-copy kernel; mbarrier suspend-time hint in ns (0: none).
-constexpr bool kPrefetchNext = true;
-constexpr bool kUseBulk = false;
-constexpr uint32_t kSuspendNs = 0;
 
 __device__ __forceinline__ void load_keys(const RowKeys& k, uint32_t* s_kh, uint32_t* s_ks) {
     if (threadIdx.x < kMaxRows) {
@@ -148,7 +144,7 @@ __global__ void __launch_bounds__(kThreads) encode_f32_vec(EncodeArgs a) {
             ++nk;
         }
         uint4 nv[4];
-        if (kPrefetchNext && nk < a.workers)
+        if (nk < a.workers)
             load_f32_task(nv, grad + (uint64_t)nk * a.n, (uint64_t)nlocal * kTaskElems, a.n, lane);
         uint32_t mask = 0;
         uint32_t my_word = 0;
@@ -213,12 +209,8 @@ __global__ void __launch_bounds__(kThreads) encode_f32_vec(EncodeArgs a) {
         }
         k = nk;
         local = nlocal;
-        if (kPrefetchNext) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) v[u] = nv[u];
-        } else if (k < a.workers) {
-            load_f32_task(v, grad + (uint64_t)k * a.n, (uint64_t)local * kTaskElems, a.n, lane);
-        }
+        for (int u = 0; u < 4; ++u) v[u] = nv[u];
     }
     if (lcount > 0)
         insert_listed<D, SL>(lpos, lval, lcount, lane, a.sketches + (uint64_t)lk * a.dw, a, s_kh, s_ks, keep);
@@ -580,181 +572,9 @@ __global__ void __launch_bounds__(kPrivThreads) encode_priv(EncodeArgs a, uint32
     }
 }
 
-// ---- 16-byte aligned rows: per-warp bulk-copy (TMA) pipeline -------------
-// Each warp owns a ring of kBulkStages shared-memory stages of 2 KB. Lane 0
-// keeps the warp's next tasks in flight with cp.async.bulk copies that
-// complete on one mbarrier per stage; the warp waits (bounded) for a stage,
-// reads it with conflict-free 16-byte shared loads, assembles and stores the
-// task's bitmap words, compacts the task's nonzero positions into a per-warp
-// list (a warp prefix sum over the words' popcounts), and then processes the
-// list 32 entries at a time: every lane takes one nonzero, re-reads its value
-// from the stage and issues its d sketch reductions. Work per task is thus
-// proportional to its nonzeros with all lanes busy, whether the nonzeros come
-// as whole rows or scattered. The gradient stream bypasses registers and the
-// load/store unit and stays in flight while the warp issues reductions.
-// Task = 2 KB of gradient: 512 fp32 (16 words) or 1024 bf16 (32 words).
-// fp32: lane l's 16-byte vector u holds positions u*128 + 4l + c;
-// bf16: lane l's vector u holds positions u*256 + 8l + c.
-constexpr int kBulkStages = 3;
-constexpr uint32_t kBulkTaskBytes = 2048;
-constexpr uint32_t kSpinLimit = 1u << 22;
-
-__device__ unsigned int g_fault = 0;  // set when a bounded wait gave up
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit) {
-    for (uint32_t it = 0; it < limit; ++it) {
-        uint32_t ok;
-        if (kSuspendNs) {
-            asm volatile(
-                "{\n\t.reg .pred p;\n\t"
-                "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-                "selp.u32 %0, 1, 0, p;\n\t}"
-                : "=r"(ok)
-                : "r"(bar), "r"(parity), "r"(kSuspendNs)
-                : "memory");
-        } else {
-            asm volatile(
-                "{\n\t.reg .pred p;\n\t"
-                "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                "selp.u32 %0, 1, 0, p;\n\t}"
-                : "=r"(ok)
-                : "r"(bar), "r"(parity)
-                : "memory");
-        }
-        if (ok) return true;
-    }
-    return false;
-}
-
-// Lane 0 of a warp: start copying task t (2 KB of gradient, or the shorter
-// tail of a worker row) into stage s; the stage's mbarrier expects its bytes.
-template <uint32_t kEsz>
-__device__ __forceinline__ void bulk_issue(const EncodeArgs& a, uint32_t t, uint32_t total, uint32_t ring_s,
-                                           uint32_t bar_s, int s, uint64_t policy) {
-    if (t >= total) return;
-    constexpr uint32_t kTE = kBulkTaskBytes / kEsz;
-    const uint32_t k = t / a.tasks_per_worker, local = t - k * a.tasks_per_worker;
-    const uint64_t e0 = (uint64_t)local * kTE;
-    const uint64_t left = a.n - e0;
-    const uint32_t bytes = (uint32_t)((left < kTE ? left : kTE) * kEsz);  // a multiple of 16
-    const unsigned char* src = static_cast<const unsigned char*>(a.grad) + ((uint64_t)k * a.n + e0) * kEsz;
-    const uint32_t bar = bar_s + 8 * s;
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
-        ::"r"(ring_s + s * kBulkTaskBytes), "l"(src), "r"(bytes), "r"(bar), "l"(policy)
-        : "memory");
-}
-
-template <int D, bool BF16>
-__global__ void __launch_bounds__(kThreads) encode_bulk(EncodeArgs a) {
-    constexpr uint32_t kEsz = BF16 ? 2u : 4u;
-    constexpr uint32_t kTE = kBulkTaskBytes / kEsz;  // positions per task
-    constexpr uint32_t kTW = kTE / 32;               // bitmap words per task
-    extern __shared__ __align__(128) unsigned char s_ring[];  // [warp][stage][2 KB]
-    __shared__ __align__(8) uint64_t s_bar[kThreads / 32][kBulkStages];
-    __shared__ uint16_t s_list[kThreads / 32][kTE];
-    __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
-    load_keys(a.keys, s_kh, s_ks);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
-    const uint32_t gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const uint32_t tpw = a.tasks_per_worker;
-    const uint32_t total = a.workers * tpw;
-    const unsigned char* ring = s_ring + (size_t)warp * kBulkStages * kBulkTaskBytes;
-    uint16_t* list = s_list[warp];
-    const uint32_t ring_s = smem_addr(ring);
-    const uint32_t bar_s = smem_addr(&s_bar[warp][0]);
-    const uint64_t keep = policy_evict_last();
-    uint64_t stream_pol = 0;
-    if (lane == 0) {
-        stream_pol = policy_evict_first();
-        for (int s = 0; s < kBulkStages; ++s)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_s + 8 * s) : "memory");
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncwarp();
-    if (lane == 0)
-        for (int s = 0; s < kBulkStages; ++s)
-            bulk_issue<kEsz>(a, gw + s * nwarps, total, ring_s, bar_s, s, stream_pol);
-    uint32_t i = 0;
-    for (uint32_t t = gw; t < total; t += nwarps, ++i) {
-        const int s = i % kBulkStages;
-        if (!mbar_wait(bar_s + 8 * s, (i / kBulkStages) & 1, kSpinLimit)) {
-            // the copy never landed: report, drain what is still in flight (bounded), leave
-            if (lane == 0) atomicOr(&g_fault, 1u);
-            for (int q = 1; q < kBulkStages; ++q)
-                mbar_wait(bar_s + 8 * ((s + q) % kBulkStages), ((i + q) / kBulkStages) & 1, 1u << 16);
-            return;
-        }
-        const uint32_t k = t / tpw, local = t - k * tpw;
-        const uint64_t e0 = (uint64_t)local * kTE;
-        const uint64_t left = a.n - e0;
-        const uint32_t cnt = (uint32_t)(left < kTE ? left : kTE);
-        const unsigned char* st = ring + s * kBulkTaskBytes;
-        // 1. nonzero bits of the lane's 4 vectors -> bitmap word `lane` of the task
-        uint32_t my_word = 0;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const uint4 v = *reinterpret_cast<const uint4*>(st + u * 512 + lane * 16);
-            const uint32_t q[4] = {v.x, v.y, v.z, v.w};
-            uint32_t bits = 0;
-            if (!BF16) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) bits |= (uint32_t)((q[c] & 0x7fffffffu) != 0) << c;
-                const int valid = (int)cnt - (u * 128 + lane * 4);
-                if (valid < 4) bits &= valid <= 0 ? 0u : ((1u << valid) - 1u);
-                uint32_t part = bits << (4 * (lane & 7));
-                part |= __shfl_xor_sync(kFull, part, 1);
-                part |= __shfl_xor_sync(kFull, part, 2);
-                part |= __shfl_xor_sync(kFull, part, 4);
-                const uint32_t got = __shfl_sync(kFull, part, (lane & 3) * 8);
-                if ((lane >> 2) == u) my_word = got;
-            } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    bits |= (uint32_t)((q[c] & 0x7fffu) != 0) << (2 * c);
-                    bits |= (uint32_t)((q[c] & 0x7fff0000u) != 0) << (2 * c + 1);
-                }
-                const int valid = (int)cnt - (u * 256 + lane * 8);
-                if (valid < 8) bits &= valid <= 0 ? 0u : ((1u << valid) - 1u);
-                uint32_t part = bits << (8 * (lane & 3));
-                part |= __shfl_xor_sync(kFull, part, 1);
-                part |= __shfl_xor_sync(kFull, part, 2);
-                const uint32_t got = __shfl_sync(kFull, part, (lane & 7) * 4);
-                if ((lane >> 3) == u) my_word = got;
-            }
-        }
-        if (lane < (int)kTW) {
-            const uint64_t wi = (uint64_t)local * kTW + lane;
-            if (wi < a.nw) a.bitmaps[(uint64_t)k * a.nw + wi] = my_word;
-        }
-        // 2. compact the set positions of the task into the warp's list
-        uint32_t nnz;
-        uint32_t at = warp_exclusive_scan(__popc(my_word), lane, &nnz);
-        for (uint32_t m = my_word; m; m &= m - 1) list[at++] = (uint16_t)(lane * 32 + __ffs(m) - 1);
-        __syncwarp();
-        // 3. every lane inserts one nonzero per round
-        float* sk = a.sketches + (uint64_t)k * a.dw;
-        for (uint32_t r = lane; r < nnz; r += 32) {
-            const uint32_t p = list[r];
-            const uint32_t bits = BF16 ? (uint32_t)(*reinterpret_cast<const uint16_t*>(st + 2 * p)) << 16
-                                       : *reinterpret_cast<const uint32_t*>(st + 4 * p);
-            insert<D, false>(sk, (uint32_t)(e0 + p), __uint_as_float(bits), a, s_kh, s_ks, keep);
-        }
-        // Every lane has consumed its reads of this stage and of the list
-        // (their values fed the reductions), so both may be overwritten.
-        __syncwarp();
-        if (lane == 0) {
-            const uint32_t nt = t + kBulkStages * nwarps;
-            if (nt > t) bulk_issue<kEsz>(a, nt, total, ring_s, bar_s, s, stream_pol);
-        }
-    }
-}
+// Fault word of s2_take_device_fault. No kernel of this library waits on
+// anything it could give up on, so nothing sets it; it stays 0.
+__device__ unsigned int g_fault = 0;
 
 // Zero `count` floats from any 4-byte-aligned address: a scalar head up to
 // the first 16-byte boundary, 16-byte stores, a scalar tail.
@@ -772,36 +592,10 @@ __global__ void __launch_bounds__(kThreads) zero_f32(float* __restrict__ p, uint
     for (uint64_t x = head + n4 * 4 + tid; x < count; x += stride) p[x] = 0.f;
 }
 
-constexpr size_t kBulkSmem = (size_t)(kThreads / 32) * kBulkStages * kBulkTaskBytes;
-
-template <int D, bool BF16>
-cudaError_t launch_bulk(const EncodeArgs& a, uint64_t tasks, cudaStream_t s) {
-    static bool configured[64] = {false};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(encode_bulk<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kBulkSmem);
-        if (e != cudaSuccess) return e;
-        configured[dev] = true;
-    }
-    const uint64_t blocks = (tasks + (kThreads / 32) - 1) / (kThreads / 32);
-    encode_bulk<D, BF16><<<grid_for(encode_bulk<D, BF16>, blocks, kBulkSmem), kThreads, kBulkSmem, s>>>(a);
-    return cudaGetLastError();
-}
-
 template <int D, bool BLK, bool SL>
 cudaError_t launch_encode_dbs(const EncodeArgs& a, int dtype, bool vec, cudaStream_t s) {
     const uint64_t tasks = (uint64_t)a.workers * a.tasks_per_worker;
     const uint64_t blocks = (tasks + (kThreads / 32) - 1) / (kThreads / 32);
-    const uint64_t esz = dtype == 0 ? 4 : 2;
-    const bool rows_aligned = (a.n * esz) % 16 == 0;
-    if (!BLK && !SL && kUseBulk && vec && rows_aligned) {
-        EncodeArgs b = a;  // bulk tasks are 2 KB of gradient
-        b.tasks_per_worker = (uint32_t)((a.n * esz + kBulkTaskBytes - 1) / kBulkTaskBytes);
-        const uint64_t btasks = (uint64_t)b.workers * b.tasks_per_worker;
-        return dtype == 0 ? launch_bulk<D, false>(b, btasks, s) : launch_bulk<D, true>(b, btasks, s);
-    }
     if (vec && dtype == 0) {
         encode_f32_vec<D, BLK, SL><<<grid_for(encode_f32_vec<D, BLK, SL>, blocks), kThreads, 0, s>>>(a);
     } else if (vec && dtype == 1) {
@@ -833,14 +627,14 @@ template <int D, int L, bool BLK, bool AGG>
 cudaError_t launch_priv_t(const EncodeArgs& a, bool only_if_preferred, bool* launched, cudaStream_t s) {
     auto kern = encode_priv<D, L, BLK, AGG>;
     const size_t smem = (size_t)a.dw * 4;
-    static bool configured[64] = {false};
+    static std::atomic<bool> configured[64];  // cudaFuncSetAttribute is idempotent
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
+    if (dev >= 0 && dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrivMaxBytes);
         if (e != cudaSuccess) return e;
-        configured[dev] = true;
+        configured[dev].store(true, std::memory_order_release);
     }
     DeviceInfo di{};
     e = device_info(&di);
