@@ -50,13 +50,14 @@ def bitmap_bytes(n: int, block: int = 0) -> int:
     return 4 * ((bits + 31) // 32)
 
 
-def algorithmic_bytes(wl: workloads.Workload, nnz_union: int, block: int = 0) -> dict:
+def algorithmic_bytes(wl: workloads.Workload, nnz_union: int, block: int = 0, compact: bool = False) -> dict:
     """Bytes each stage must move at minimum (each structure read/written once).
 
     encode: read grad, write W bitmaps and W sketches;
     reduce: read W bitmaps and W sketches, write one bitmap and one sketch;
     decode: read the bitmap, read at most the sketch (d gathers per set bit,
-            counted up to one full read), write the dense output.
+            counted up to one full read), write the dense output (compact:
+            an index and a value per set position).
     """
     W, n, d, w = wl.W, wl.n, wl.d, wl.w
     E = wl.elem_bytes
@@ -64,7 +65,7 @@ def algorithmic_bytes(wl: workloads.Workload, nnz_union: int, block: int = 0) ->
     SK = 4 * d * w
     enc = W * n * E + W * BM + W * SK
     red = W * (SK + BM) + SK + BM
-    dec = BM + min(SK, 4 * d * nnz_union) + 4 * n
+    dec = BM + min(SK, 4 * d * nnz_union) + (8 * nnz_union if compact else 4 * n)
     return {"encode": enc, "reduce": red, "decode": dec, "total": enc + red + dec}
 
 
@@ -85,7 +86,7 @@ def l2_sector_ops_fused(wl: workloads.Workload, nnz_union: int) -> dict:
     return {"encode_reduce_fused": fused, "decode": ops["decode"], "total": fused + ops["decode"]}
 
 
-def l2_sector_ops(wl: workloads.Workload, nnz_union: int, block: int = 0) -> dict:
+def l2_sector_ops(wl: workloads.Workload, nnz_union: int, block: int = 0, compact: bool = False) -> dict:
     """32-byte L2 sector operations each stage issues at minimum.
 
     Streams count one operation per 32-byte sector; every scattered 4-byte
@@ -102,7 +103,7 @@ def l2_sector_ops(wl: workloads.Workload, nnz_union: int, block: int = 0) -> dic
     nnz = sum(wl.nnz_per_worker)
     enc = sec(W * n * wl.elem_bytes) + W * sec(BM) + W * sec(SK) + nnz * d
     red = W * (sec(SK) + sec(BM)) + sec(SK) + sec(BM)
-    dec = sec(BM) + nnz_union * d + sec(4 * n)
+    dec = sec(BM) + nnz_union * d + (sec(8 * nnz_union) if compact else sec(4 * n))
     return {"encode": enc, "reduce": red, "decode": dec, "total": enc + red + dec}
 
 
@@ -315,7 +316,17 @@ def run_ours(args, wl, world, rank, local):
         sketches = torch.empty((W, d, w), dtype=torch.float32, device=dev)
     bitmap = torch.empty(s2.nwords(nbits), dtype=torch.int32, device=dev)
     sketch = torch.empty((d, w), dtype=torch.float32, device=dev)
-    out = torch.empty(n, dtype=torch.float32, device=dev)
+    compact = args.decode == "compact"
+    if compact:
+        if blk:
+            raise SystemExit("--decode compact takes the element bitmap")
+        cidx = torch.empty(max(nnz_u, 1), dtype=torch.int32, device=dev)
+        cval = torch.empty(max(nnz_u, 1), dtype=torch.float32, device=dev)
+        ccnt = torch.empty(1, dtype=torch.int64, device=dev)
+        cws = torch.empty(max(s2.s2_decode_workspace_size(n), 1), dtype=torch.uint8, device=dev)
+        out = None
+    else:
+        out = torch.empty(n, dtype=torch.float32, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -330,6 +341,8 @@ def run_ours(args, wl, world, rank, local):
     def decode():
         if blk:
             s2.s2_decode_dense_blocks(bitmap, sketch, n, blk, d, w, seed, out)
+        elif compact:
+            s2.s2_decode_compact(bitmap, sketch, n, d, w, seed, cidx, cval, ccnt, cws)
         else:
             s2.s2_decode_dense(bitmap, sketch, n, d, w, seed, out)
 
@@ -382,12 +395,12 @@ def run_ours(args, wl, world, rank, local):
     elapsed, units = combine_over_ranks(total_ms / 1e3, float(W * n * K), world, dev)
     value = units / elapsed / 1e9
 
-    by = algorithmic_bytes(wl, nnz_u, blk)
+    by = algorithmic_bytes(wl, nnz_u, blk, compact)
     peaks = measured_peaks()
     peak = peaks["hbm_gbs"]
     enc_s = enc_ms / 1e3 / K
     n_enc = encode_launches(wl, l2)
-    n_dec = dense_decode_launches(n, l2)
+    n_dec = 3 if args.decode == "compact" else dense_decode_launches(n, l2)
     ach_enc = by["encode"] / enc_s / 1e9
     path_gbs = by["total"] / (total_ms / 1e3 / K) / 1e9
     traffic = recorded_traffic(args.config)
@@ -421,7 +434,7 @@ def run_ours(args, wl, world, rank, local):
         "gpu_launches": K * (n_enc + 1 + n_dec),
         "wall_ms_timed_region": round(wall * 1e3, 3),
     }
-    ops = l2_sector_ops(wl, nnz_u, blk)
+    ops = l2_sector_ops(wl, nnz_u, blk, compact)
     ceil = measured_ceilings()
     step_s = total_ms / 1e3 / K
     l2 = {"unit": "G sector ops/s", "ops_per_step": ops, "achieved": round(ops["total"] / step_s / 1e9, 1)}
@@ -430,7 +443,8 @@ def run_ours(args, wl, world, rank, local):
         l2.update(peak=c, frac=round(ops["total"] / step_s / 1e9 / c, 4),
                   peak_source="scattered red.f32 rate measured by bench.py --ceilings (profiles/ceilings_gb300.json)")
     res["l2_roofline"] = l2
-    res["config"]["mode"] = "per_worker (encode_batched + reduce + decode_dense)"
+    res["config"]["mode"] = ("per_worker (encode_batched + reduce + decode_compact)" if compact else
+                             "per_worker (encode_batched + reduce + decode_dense)")
     if blk:
         res["config"]["mode"] = f"per_worker, block bitmap of {blk} positions (encode_batched_blocks + reduce + decode_dense_blocks)"
         res["gpu_launches"] = K * (n_enc + 1 + 1 + n_dec)  # + the block bitmaps' zero fill
@@ -843,6 +857,8 @@ def main(argv=None):
     ap.add_argument("--mode", choices=["per_worker", "fused", "allgather"], default="per_worker",
                     help="per_worker: the simulated data-parallel path (default); fused: encode_reduce_fused + "
                          "decode; allgather: the sparse AllGather baseline (exact sum) on the same workload")
+    ap.add_argument("--decode", choices=["dense", "compact"], default="dense",
+                    help="decode output: dense [n] (default) or compacted (index, value) pairs")
     ap.add_argument("--block", type=int, default=0,
                     help="positions per bitmap bit (a multiple of 32; 0 = one bit per position, the default)")
     ap.add_argument("--workers", type=int, default=None,

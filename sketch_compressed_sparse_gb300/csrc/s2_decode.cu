@@ -15,8 +15,9 @@
 //
 // The compacted output uses three kernels and no inter-block waiting:
 // per-tile popcounts, one block that scans the tile totals (and writes the
-// final count), and a writer that recomputes the in-tile offsets with warp
-// scans and writes (index, value) pairs in ascending order.
+// final count), and a writer with one warp per task that recomputes its rank
+// inside the tile from the bitmap and writes (index, value) pairs in
+// ascending order.
 #include <mutex>
 
 #include "s2_internal.h"
@@ -168,32 +169,29 @@ __global__ void __launch_bounds__(kThreads) decode_dense_kernel(DecodeArgs a, fl
 
 // ---- compacted output -------------------------------------------------------
 
-__device__ __forceinline__ uint32_t block_sum(uint32_t v, uint32_t* s_tmp) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-    if (lane == 0) s_tmp[warp] = v;
-    __syncthreads();
-    uint32_t tot = 0;
-    if (threadIdx.x < 32) {
-        tot = (lane < (int)(blockDim.x >> 5)) ? s_tmp[lane] : 0u;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(kFull, tot, o);
-    }
-    __syncthreads();
-    return tot;  // valid in thread 0
-}
-
-// Set bits per tile of kCompactTileWords words (one word per thread).
+// Set bits per tile of kCompactTileWords words (one word per thread), and the
+// set bits of the tile's tasks before each task (its in-tile prefix).
+static_assert(kCompactTileWords == kThreads, "one thread per word of a tile");
 __global__ void __launch_bounds__(kThreads)
     compact_count_kernel(const uint32_t* __restrict__ bitmap, uint64_t nw, uint64_t n, uint64_t tiles,
-                         uint32_t* __restrict__ counts) {
-    __shared__ uint32_t s_tmp[kThreads / 32];
+                         uint32_t* __restrict__ counts, uint16_t* __restrict__ task_prefix) {
+    constexpr int kTasksPerTile = kCompactTileWords / kTaskWords;
+    __shared__ uint32_t s_task[kTasksPerTile];
     for (uint64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
         const uint64_t wi = t * kCompactTileWords + threadIdx.x;
-        const uint32_t c = __popc(load_word(bitmap, wi, nw, n));
-        const uint32_t tot = block_sum(c, s_tmp);
-        if (threadIdx.x == 0) counts[t] = tot;
+        uint32_t c = __popc(load_word(bitmap, wi, nw, n));
+        // the 16 words of a task are a half warp
+#pragma unroll
+        for (int o = kTaskWords / 2; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
+        if ((threadIdx.x & (kTaskWords - 1)) == 0) s_task[threadIdx.x / kTaskWords] = c;
+        __syncthreads();
+        if (threadIdx.x < kTasksPerTile) {
+            uint32_t before = 0;
+            for (int q = 0; q < (int)threadIdx.x; ++q) before += s_task[q];
+            task_prefix[t * kTasksPerTile + threadIdx.x] = (uint16_t)before;  // at most 15 * 512
+            if (threadIdx.x == kTasksPerTile - 1) counts[t] = before + s_task[kTasksPerTile - 1];
+        }
+        __syncthreads();  // s_task is rewritten by the next tile
     }
 }
 
@@ -236,71 +234,82 @@ __global__ void __launch_bounds__(kScanThreads)
     if (threadIdx.x == kScanThreads - 1) *count_out = s_warp[31];
 }
 
-// Writer: block = tile of 256 words = 16 tasks of 512 positions; warp w
-// handles tasks 2w and 2w+1 of the tile.
+// Writer, one warp per task of 512 positions (grid-stride, like the dense
+// decode), no block-wide synchronisation. Tiles without a set position are
+// skipped from their count alone; a task's first rank is its tile's offset
+// plus the in-tile prefix the count kernel stored for it. Within a task each
+// lane walks its set slots kPop at a time, writing (index, value) at the
+// position's rank: task prefix + earlier words of the task + earlier bits of
+// the word.
+template <int D>
+__device__ __forceinline__ void compact_task(const DecodeArgs& a, uint64_t t, uint32_t my_word, uint64_t tbase,
+                                             int lane, const uint32_t* s_kh, const uint32_t* s_ks, uint64_t keep,
+                                             uint32_t* __restrict__ idx_out, float* __restrict__ val_out,
+                                             uint64_t capacity) {
+    const uint32_t cnt = __popc(my_word);
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const uint32_t excl = incl - cnt;
+    uint32_t wv[4], wo[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        wv[u] = __shfl_sync(kFull, my_word, u * 4 + (lane >> 3));
+        wo[u] = __shfl_sync(kFull, excl, u * 4 + (lane >> 3));
+    }
+    const uint64_t e0 = t * kTaskElems;
+    uint32_t mask = lane_mask(my_word, lane);
+    while (mask) {
+        int sl[kPop];
+        bool ok[kPop];
+#pragma unroll
+        for (int q = 0; q < kPop; ++q) {
+            ok[q] = mask != 0;
+            sl[q] = ok[q] ? __ffs(mask) - 1 : (q ? sl[0] : 0);
+            if (ok[q]) mask &= mask - 1;
+        }
+        float ev[kPop][(D > 0 ? D : kMaxRows)];
+#pragma unroll
+        for (int q = 0; q < kPop; ++q)
+            gather_hint<D>(ev[q], a.sketch, (uint32_t)e0 + slot_pos(sl[q], lane), a.d, a.w, s_kh, s_ks, keep);
+#pragma unroll
+        for (int q = 0; q < kPop; ++q) {
+            if (!ok[q]) continue;
+            const int u = sl[q] >> 2;
+            const uint32_t bitpos = 4 * (lane & 7) + (sl[q] & 3);
+            const uint32_t word = u == 0 ? wv[0] : (u == 1 ? wv[1] : (u == 2 ? wv[2] : wv[3]));
+            const uint32_t woff = u == 0 ? wo[0] : (u == 1 ? wo[1] : (u == 2 ? wo[2] : wo[3]));
+            const uint64_t off = tbase + woff + __popc(word & ((1u << bitpos) - 1u));
+            if (off < capacity) {
+                idx_out[off] = (uint32_t)e0 + slot_pos(sl[q], lane);
+                val_out[off] = a.scale * median_rows<D>(ev[q], a.d);
+            }
+        }
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads)
-    compact_write_kernel(DecodeArgs a, uint64_t tiles, const uint32_t* __restrict__ offsets, uint32_t* __restrict__ idx_out,
-                         float* __restrict__ val_out, uint64_t capacity) {
+    compact_write_kernel(DecodeArgs a, const uint32_t* __restrict__ tile_counts,
+                         const uint32_t* __restrict__ offsets, const uint16_t* __restrict__ task_prefix,
+                         uint32_t* __restrict__ idx_out, float* __restrict__ val_out, uint64_t capacity) {
     __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
-    __shared__ uint32_t s_task[16];
     load_keys(a.keys, s_kh, s_ks);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr uint32_t kTasksPerTile = kCompactTileWords / kTaskWords;
+    const int lane = threadIdx.x & 31;
     const uint64_t keep = policy_evict_last();
-    for (uint64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
-        uint32_t words[2], excl[2], tot[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint64_t task = tile * 16 + warp * 2 + h;
-            const uint64_t wi = task * kTaskWords + lane;
-            words[h] = lane < kTaskWords ? load_word(a.bitmap, wi, a.nw, a.n) : 0u;
-            const uint32_t c = __popc(words[h]);
-            uint32_t incl = c;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                uint32_t y = __shfl_up_sync(kFull, incl, o);
-                if (lane >= o) incl += y;
-            }
-            excl[h] = incl - c;
-            tot[h] = __shfl_sync(kFull, incl, 31);
-        }
-        if (lane == 0) {
-            s_task[warp * 2] = tot[0];
-            s_task[warp * 2 + 1] = tot[1];
-        }
-        __syncthreads();
-        uint32_t base = offsets[tile];
-        for (int q = 0; q < warp * 2; ++q) base += s_task[q];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint64_t task = tile * 16 + warp * 2 + h;
-            const uint64_t e0 = task * kTaskElems;
-            const uint32_t tbase = base + (h ? tot[0] : 0u);
-            uint32_t mask = lane_mask(words[h], lane);
-            uint32_t wv[4], wo[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                wv[u] = __shfl_sync(kFull, words[h], u * 4 + (lane >> 3));
-                wo[u] = __shfl_sync(kFull, excl[h], u * 4 + (lane >> 3));
-            }
-            while (mask) {
-                const int s0 = __ffs(mask) - 1;
-                mask &= mask - 1;
-                const int u = s0 >> 2;
-                const uint32_t bitpos = 4 * (lane & 7) + (s0 & 3);
-                const uint32_t word = u == 0 ? wv[0] : (u == 1 ? wv[1] : (u == 2 ? wv[2] : wv[3]));
-                const uint32_t woff = u == 0 ? wo[0] : (u == 1 ? wo[1] : (u == 2 ? wo[2] : wo[3]));
-                const uint64_t off = (uint64_t)tbase + woff + __popc(word & ((1u << bitpos) - 1u));
-                const uint32_t i = (uint32_t)e0 + slot_pos(s0, lane);
-                if (off < capacity) {
-                    float ev[(D > 0 ? D : kMaxRows)];
-                    gather_hint<D>(ev, a.sketch, i, a.d, a.w, s_kh, s_ks, keep);
-                    idx_out[off] = i;
-                    val_out[off] = a.scale * median_rows<D>(ev, a.d);
-                }
-            }
-        }
-        __syncthreads();  // s_task is rewritten by the next tile
+    const uint64_t ntasks = (a.n + kTaskElems - 1) / kTaskElems;
+    const uint64_t nwarps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
+    for (uint64_t t = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < ntasks; t += nwarps) {
+        const uint64_t tile = t / kTasksPerTile;
+        if (__ldg(tile_counts + tile) == 0) continue;
+        const uint32_t my_word = lane < kTaskWords ? load_word(a.bitmap, t * kTaskWords + lane, a.nw, a.n) : 0u;
+        if (!__any_sync(kFull, my_word != 0)) continue;
+        compact_task<D>(a, t, my_word, (uint64_t)offsets[tile] + __ldg(task_prefix + t), lane, s_kh, s_ks, keep,
+                        idx_out, val_out, capacity);
     }
 }
 
@@ -330,10 +339,13 @@ cudaError_t launch_dense_d(const DecodeArgs& a, float* out, cudaStream_t s) {
 }
 
 template <int D>
-cudaError_t launch_compact_write_d(const DecodeArgs& a, uint64_t tiles, const uint32_t* offsets,
-                                   uint32_t* idx_out, float* val_out, uint64_t capacity, cudaStream_t s) {
-    compact_write_kernel<D><<<grid_for(compact_write_kernel<D>, tiles), kThreads, 0, s>>>(
-        a, tiles, offsets, idx_out, val_out, capacity);
+cudaError_t launch_compact_write_d(const DecodeArgs& a, const uint32_t* tile_counts, const uint32_t* offsets,
+                                   const uint16_t* task_prefix, uint32_t* idx_out, float* val_out,
+                                   uint64_t capacity, cudaStream_t s) {
+    const uint64_t tasks = (a.n + kTaskElems - 1) / kTaskElems;
+    const uint64_t blocks = (tasks + (kThreads / 32) - 1) / (kThreads / 32);
+    compact_write_kernel<D><<<grid_for(compact_write_kernel<D>, blocks), kThreads, 0, s>>>(
+        a, tile_counts, offsets, task_prefix, idx_out, val_out, capacity);
     return cudaGetLastError();
 }
 
@@ -357,19 +369,24 @@ cudaError_t launch_tile_scan(const uint32_t* counts, uint64_t tiles, uint32_t* o
 
 uint64_t compact_tiles(uint64_t nw) { return (nw + kCompactTileWords - 1) / kCompactTileWords; }
 
+// Workspace of the compacted decode: tile counts, tile offsets (each rounded
+// to 256 bytes), then the in-tile prefix of every task (16-bit).
 size_t compact_workspace_bytes(uint64_t n) {
     const uint64_t tiles = compact_tiles((n + 31) / 32);
     const uint64_t one = (tiles * sizeof(uint32_t) + 255) / 256 * 256;
-    return (size_t)(2 * one);
+    const uint64_t prefix = (tiles * (kCompactTileWords / kTaskWords) * sizeof(uint16_t) + 255) / 256 * 256;
+    return (size_t)(2 * one + prefix);
 }
 
 cudaError_t launch_decode_compact(const DecodeArgs& a, uint32_t* idx_out, float* val_out, uint64_t capacity,
                                   unsigned long long* count_out, uint32_t* tile_counts, uint32_t* tile_offsets,
                                   cudaStream_t s) {
     const uint64_t tiles = compact_tiles(a.nw);
+    // the task prefixes follow the tile offsets (see compact_workspace_bytes)
+    uint16_t* task_prefix = reinterpret_cast<uint16_t*>(tile_offsets + (tiles * sizeof(uint32_t) + 255) / 256 * 64);
     if (tiles > 0) {
         compact_count_kernel<<<grid_for(compact_count_kernel, tiles), kThreads, 0, s>>>(a.bitmap, a.nw, a.n,
-                                                                                        tiles, tile_counts);
+                                                                                        tiles, tile_counts, task_prefix);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -377,23 +394,26 @@ cudaError_t launch_decode_compact(const DecodeArgs& a, uint32_t* idx_out, float*
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || tiles == 0) return e;
     switch (a.d) {
-        case 3: return launch_compact_write_d<3>(a, tiles, tile_offsets, idx_out, val_out, capacity, s);
-        case 5: return launch_compact_write_d<5>(a, tiles, tile_offsets, idx_out, val_out, capacity, s);
-        case 1: return launch_compact_write_d<1>(a, tiles, tile_offsets, idx_out, val_out, capacity, s);
-        default: return launch_compact_write_d<0>(a, tiles, tile_offsets, idx_out, val_out, capacity, s);
+        case 3: return launch_compact_write_d<3>(a, tile_counts, tile_offsets, task_prefix, idx_out, val_out, capacity, s);
+        case 5: return launch_compact_write_d<5>(a, tile_counts, tile_offsets, task_prefix, idx_out, val_out, capacity, s);
+        case 1: return launch_compact_write_d<1>(a, tile_counts, tile_offsets, task_prefix, idx_out, val_out, capacity, s);
+        default: return launch_compact_write_d<0>(a, tile_counts, tile_offsets, task_prefix, idx_out, val_out, capacity, s);
     }
 }
 
 // ---- compaction with library-owned scratch -----------------------------------
 // s2_decode_compact_noalloc runs the same three kernels as s2_decode_compact,
-// but its tile counts and tile offsets live in this file-scope device array
-// instead of a caller workspace. It covers n up to kNoAllocMaxN positions
-// (2^30: 131,072 tiles, 1 MiB); every GPU that loads the library holds the
+// but its tile counts, tile offsets and task prefixes live in this
+// file-scope device array instead of a caller workspace. It covers n up to
+// kNoAllocMaxN positions (2^30: 131,072 tiles; 1 MiB of counts and offsets,
+// 4 MiB of 16-bit task prefixes); every GPU that loads the library holds the
 // array until the process exits. Nothing in it has to start at zero: a call
-// writes every count it later scans and every offset it later reads.
+// writes every count it later scans and every offset or prefix it later
+// reads. The prefixes of a call start right after its own tile offsets.
 constexpr uint64_t kNoAllocMaxN = 1ull << 30;
 constexpr uint64_t kNoAllocMaxTiles = (kNoAllocMaxN / 32) / kCompactTileWords;
-static __device__ __align__(256) uint32_t g_noalloc_compact_scratch[2 * kNoAllocMaxTiles];
+static __device__ __align__(256) uint32_t
+    g_noalloc_compact_scratch[2 * kNoAllocMaxTiles + (kNoAllocMaxTiles * (kCompactTileWords / kTaskWords)) / 2 + 64];
 
 uint64_t noalloc_compact_max_n() { return kNoAllocMaxN; }
 
