@@ -280,8 +280,9 @@ S2_API s2_status s2_decode_compact(const uint32_t *bitmap, const float *sketch, 
  * that keeps no state between calls in which a workspace could live.
  *
  * Same arguments, results and errors as s2_decode_compact, minus the
- * workspace. The scratch it needs (per-tile counts and offsets) is a fixed
- * 1 MiB array inside the library, allocated once per GPU when the library's
+ * workspace. The scratch it needs (per-tile counts and offsets, per-task
+ * prefixes) is a fixed 5 MiB array inside the library, allocated once per
+ * GPU when the library's
  * device code is first loaded there and held until the process exits; the
  * call itself allocates nothing. It accepts n up to 2^30 positions and
  * returns S2_ERR_UNSUPPORTED beyond that.
