@@ -282,9 +282,8 @@ S2_API s2_status s2_decode_compact(const uint32_t *bitmap, const float *sketch, 
  * Same arguments, results and errors as s2_decode_compact, minus the
  * workspace. The scratch it needs (per-tile counts and offsets, per-task
  * prefixes) is a fixed 5 MiB array inside the library, allocated once per
- * GPU when the library's
- * device code is first loaded there and held until the process exits; the
- * call itself allocates nothing. It accepts n up to 2^30 positions and
+ * GPU when the library's device code is first loaded there and held until
+ * the process exits; the call itself allocates nothing. It accepts n up to 2^30 positions and
  * returns S2_ERR_UNSUPPORTED beyond that.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) and caches it; make that first call before any
