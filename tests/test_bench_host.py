@@ -52,6 +52,34 @@ def test_encode_launch_groups():
     assert bench.encode_launches(wl, 126 << 20) == 2
 
 
+def test_encode_launches_follow_the_path_choice():
+    L2 = 135_528_448
+    # a 3 KiB sketch with 4096 positions per bucket and more: the shared-memory
+    # path, a zero fill and one encode
+    wl = workloads.Workload("s", 8, 1 << 22, 3, 256, 0, "f32", [], [])
+    assert bench.encode_launches(wl, L2) == 2
+    # few positions per bucket: the L2 path (one group)
+    wl = workloads.Workload("t", 2, 4096, 3, 256, 0, "f32", [], [])
+    assert bench.encode_launches(wl, L2) == 2
+    # a 160 MiB sketch: one worker at a time in two slice passes
+    wl = workloads.Workload("b", 8, 1 << 27, 5, 1 << 23, 0, "f32", [], [])
+    assert bench.encode_launches(wl, L2) == 2 * 8 * 2
+
+
+def test_dense_decode_launches():
+    L2 = 135_528_448
+    assert bench.dense_decode_launches(33_278 * 512, L2) == 1
+    assert bench.dense_decode_launches(267_735 * 1024, L2) == 2  # 1.1 GB of output: zeros first
+
+
+def test_compact_decode_accounting():
+    wl = workloads.Workload("e", 8, 33_278 * 512, 5, 1 << 20, 0, "f32", [], [])
+    dense = bench.algorithmic_bytes(wl, 4_466_688)
+    comp = bench.algorithmic_bytes(wl, 4_466_688, compact=True)
+    assert dense["decode"] - comp["decode"] == 4 * wl.n - 8 * 4_466_688
+    assert dense["encode"] == comp["encode"] and dense["reduce"] == comp["reduce"]
+
+
 def test_reference_arm_line(capsys):
     assert bench.main(["--impl", "reference", "--config", "tiny", "--steps", "2", "--warmup", "1"]) == 0
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
