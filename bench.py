@@ -560,7 +560,8 @@ def run_blocktopk(args, world, rank, local):
         "path_roofline": {"bound": "hbm", "achieved": round(total_b / (step_ms / 1e3) / 1e9, 1), "peak": peak,
                           "unit": "GB/s", "frac": round(total_b / (step_ms / 1e3) / 1e9 / peak, 4),
                           "algorithmic_bytes_per_step": total_b},
-        "gpu_launches": Ksteps * (3 + encode_launches(workloads.Workload("x", W, n, d, w, 0, "f32", [], []),
+        # Top-K: norms, histogram zero fill, 4 radix passes, equal counts, keep, apply
+        "gpu_launches": Ksteps * (9 + encode_launches(workloads.Workload("x", W, n, d, w, 0, "f32", [], []),
                                                       int(torch.cuda.get_device_properties(dev).L2_cache_size)) + 2),
         "clocks": clk.summary(),
     }

@@ -9,16 +9,21 @@
 // butterfly), so that which blocks are kept -- an integer decision -- does
 // not depend on scheduling; the K-th largest norm by a 4-pass 8-bit radix
 // select over the norms' bit patterns (non-negative floats order like their
-// bits), ties broken towards the lower block index by an ordered block-wide
-// scan; finally sparse = acc on kept blocks and residual = acc elsewhere.
-// Three kernels, no inter-block waiting.
+// bits), ties broken towards the lower block index; finally sparse = acc on
+// kept blocks and residual = acc elsewhere.
+//
+// The select runs on many thread blocks per worker: each radix pass is one
+// launch that adds the digit counts of its slice of the norms into a global
+// 256-bin histogram per worker (every block first replays the earlier
+// passes' histograms to find the prefix it must match); a counting launch
+// and a marking launch then keep every norm above the final threshold and,
+// of the norms equal to it, the first ones in index order (each block starts
+// its rank after the equal norms of the blocks before it). No launch waits on
+// another block.
 #include "s2_internal.h"
 
 namespace s2 {
 namespace {
-
-constexpr int kSelThreads = 1024;
-constexpr int kSelUnroll = 8;
 
 // Squared norm of block x of worker k, one warp per (k, x) task.
 __global__ void __launch_bounds__(kThreads)
@@ -43,78 +48,150 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-// One block of kSelThreads threads per worker: keep[k][x] = 1 for the K
-// blocks of largest norm (ties: lower index).
+constexpr int kSelThreads = 256;
+constexpr int kSelPerThread = 16;                       // norms per thread and launch
+constexpr uint64_t kSelSlice = (uint64_t)kSelThreads * kSelPerThread;  // norms per block
+static_assert(kSelThreads == 256, "one thread per histogram bin");
+
+// The radix state after `passes` passes of worker k: the digits fixed so far
+// (prefix under pmask) and how many norms equal to that prefix are still to
+// be kept. hist: [4][W][256] digit counts of the passes (pass-major).
+__device__ void select_state(const uint32_t* __restrict__ hist, uint32_t W, uint32_t k, int passes, uint64_t K,
+                             uint32_t* prefix, uint32_t* pmask, uint64_t* rest) {
+    uint32_t pf = 0, pm = 0;
+    uint64_t r = K;
+    for (int p = 0; p < passes; ++p) {
+        const uint32_t* h = hist + ((uint64_t)p * W + k) * 256;
+        const int shift = 24 - 8 * p;
+        uint64_t above = 0;
+        int dg = 255;
+        for (; dg > 0; --dg) {
+            if (above + h[dg] >= r) break;
+            above += h[dg];
+        }
+        pf |= (uint32_t)dg << shift;
+        pm |= 255u << shift;
+        r -= above;
+    }
+    *prefix = pf;
+    *pmask = pm;
+    *rest = r;
+}
+
+// Pass `pass` of the radix select: digit counts of the norms that match the
+// prefix fixed by the earlier passes. Grid: (W, slices).
 __global__ void __launch_bounds__(kSelThreads)
-    topk_select_kernel(const float* __restrict__ norms, uint64_t nb, uint64_t K, uint8_t* __restrict__ keep) {
+    topk_hist_kernel(const float* __restrict__ norms, uint64_t nb, uint64_t K, uint32_t W, int pass,
+                     uint32_t* __restrict__ hist) {
     __shared__ uint32_t s_hist[256];
-    __shared__ uint32_t s_digit, s_rest;
+    __shared__ uint32_t s_prefix, s_pmask;
+    const uint32_t k = blockIdx.x;
+    if (threadIdx.x == 0) {
+        uint64_t rest;
+        select_state(hist, W, k, pass, K, &s_prefix, &s_pmask, &rest);
+    }
+    s_hist[threadIdx.x] = 0;  // kSelThreads == 256 bins
+    __syncthreads();
+    const uint32_t prefix = s_prefix, pmask = s_pmask;
+    const int shift = 24 - 8 * pass;
+    const uint32_t* key = reinterpret_cast<const uint32_t*>(norms) + (uint64_t)k * nb;
+    const uint64_t x0 = (uint64_t)blockIdx.y * kSelSlice;
+    uint32_t v[kSelPerThread];
+#pragma unroll
+    for (int q = 0; q < kSelPerThread; ++q) {  // independent loads first
+        const uint64_t x = x0 + (uint64_t)q * kSelThreads + threadIdx.x;
+        v[q] = x < nb ? __ldg(key + x) : 0u;
+    }
+#pragma unroll
+    for (int q = 0; q < kSelPerThread; ++q) {
+        const uint64_t x = x0 + (uint64_t)q * kSelThreads + threadIdx.x;
+        if (x < nb && (v[q] & pmask) == prefix) atomicAdd(&s_hist[(v[q] >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    const uint32_t c = s_hist[threadIdx.x];
+    if (c) atomicAdd(hist + ((uint64_t)pass * W + k) * 256 + threadIdx.x, c);
+}
+
+// Norms equal to the final threshold in each slice. Grid: (W, slices).
+__global__ void __launch_bounds__(kSelThreads)
+    topk_eq_kernel(const float* __restrict__ norms, uint64_t nb, uint64_t K, uint32_t W,
+                   const uint32_t* __restrict__ hist, uint32_t* __restrict__ eq_counts) {
+    __shared__ uint32_t s_thr;
+    __shared__ uint32_t s_warp[kSelThreads / 32];
+    const uint32_t k = blockIdx.x;
+    if (threadIdx.x == 0) {
+        uint32_t pm;
+        uint64_t rest;
+        select_state(hist, W, k, 4, K, &s_thr, &pm, &rest);
+    }
+    __syncthreads();
+    const uint32_t thr = s_thr;
+    const uint32_t* key = reinterpret_cast<const uint32_t*>(norms) + (uint64_t)k * nb;
+    const uint64_t x0 = (uint64_t)blockIdx.y * kSelSlice;
+    uint32_t c = 0;
+#pragma unroll
+    for (int q = 0; q < kSelPerThread; ++q) {
+        const uint64_t x = x0 + (uint64_t)q * kSelThreads + threadIdx.x;
+        c += (x < nb && __ldg(key + x) == thr) ? 1u : 0u;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
+    if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = c;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t t = 0;
+        for (int w = 0; w < kSelThreads / 32; ++w) t += s_warp[w];
+        eq_counts[(uint64_t)k * gridDim.y + blockIdx.y] = t;
+    }
+}
+
+// keep[k][x] = 1 for the K blocks of largest norm (ties: lower index).
+// Grid: (W, slices).
+__global__ void __launch_bounds__(kSelThreads)
+    topk_keep_kernel(const float* __restrict__ norms, uint64_t nb, uint64_t K, uint32_t W,
+                     const uint32_t* __restrict__ hist, const uint32_t* __restrict__ eq_counts,
+                     uint8_t* __restrict__ keep) {
+    __shared__ uint32_t s_thr;
+    __shared__ unsigned long long s_rest, s_base;
     __shared__ uint32_t s_scan[kSelThreads / 32];
     const uint32_t k = blockIdx.x;
-    const uint32_t* key = reinterpret_cast<const uint32_t*>(norms) + (uint64_t)k * nb;
-    uint8_t* kp = keep + (uint64_t)k * nb;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint64_t x0 = (uint64_t)blockIdx.y * kSelSlice;
+    uint8_t* kp = keep + (uint64_t)k * nb;
     if (K == 0 || K >= nb) {
-        for (uint64_t x = threadIdx.x; x < nb; x += kSelThreads) kp[x] = K == 0 ? 0 : 1;
+        for (int q = 0; q < kSelPerThread; ++q) {
+            const uint64_t x = x0 + (uint64_t)q * kSelThreads + threadIdx.x;
+            if (x < nb) kp[x] = K == 0 ? 0 : 1;
+        }
         return;
     }
-    // radix select of the K-th largest key: prefix/mask narrow down, `rest`
-    // counts how many keys equal to the final prefix are to be kept
-    uint32_t prefix = 0, pmask = 0;
-    uint64_t rest = K;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int b = threadIdx.x; b < 256; b += kSelThreads) s_hist[b] = 0;
-        __syncthreads();
-        for (uint64_t x0 = 0; x0 < nb; x0 += kSelUnroll * kSelThreads) {
-            uint32_t v[kSelUnroll];
-#pragma unroll
-            for (int q = 0; q < kSelUnroll; ++q) {  // independent loads first
-                const uint64_t x = x0 + q * kSelThreads + threadIdx.x;
-                v[q] = x < nb ? key[x] : 0u;
-            }
-#pragma unroll
-            for (int q = 0; q < kSelUnroll; ++q) {
-                const uint64_t x = x0 + q * kSelThreads + threadIdx.x;
-                const bool in = x < nb && (v[q] & pmask) == prefix;
-                const uint32_t dg = in ? (v[q] >> shift) & 255u : 256u;  // 256: no vote
-                const unsigned grp = __match_any_sync(kFull, dg);
-                if (in && __ffs(grp) - 1 == lane) atomicAdd(&s_hist[dg], (uint32_t)__popc(grp));
-            }
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            uint64_t above = 0;
-            int dg = 255;
-            for (; dg > 0; --dg) {
-                if (above + s_hist[dg] >= rest) break;
-                above += s_hist[dg];
-            }
-            s_digit = (uint32_t)dg;
-            s_rest = (uint32_t)(rest - above);
-        }
-        __syncthreads();
-        prefix |= s_digit << shift;
-        pmask |= 255u << shift;
-        rest = s_rest;
-        __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t pm;
+        uint64_t rest;
+        select_state(hist, W, k, 4, K, &s_thr, &pm, &rest);
+        s_rest = rest;
+        unsigned long long base = 0;  // equal norms in the slices before this one
+        for (uint32_t b = 0; b < blockIdx.y; ++b) base += eq_counts[(uint64_t)k * gridDim.y + b];
+        s_base = base;
     }
-    // keep every key above the threshold and the first `rest` keys equal to
-    // it in index order
-    const uint32_t thr = prefix;
-    uint32_t taken = 0;  // equal keys already kept (uniform across the block)
-    for (uint64_t x0 = 0; x0 < nb; x0 += kSelThreads) {
-        const uint64_t x = x0 + threadIdx.x;
-        const uint32_t v = x < nb ? key[x] : 0u;
+    __syncthreads();
+    const uint32_t thr = s_thr;
+    const uint64_t rest = s_rest;
+    uint64_t taken = s_base;  // equal norms before the current chunk (uniform across the block)
+    const uint32_t* key = reinterpret_cast<const uint32_t*>(norms) + (uint64_t)k * nb;
+    for (int q = 0; q < kSelPerThread; ++q) {  // chunks of kSelThreads norms in index order
+        const uint64_t x = x0 + (uint64_t)q * kSelThreads + threadIdx.x;
+        const uint32_t v = x < nb ? __ldg(key + x) : 0u;
         const bool eq = x < nb && v == thr;
         const unsigned bal = __ballot_sync(kFull, eq);
         if (lane == 0) s_scan[warp] = __popc(bal);
         __syncthreads();
-        uint32_t before = taken;
-        for (int q = 0; q < warp; ++q) before += s_scan[q];
+        uint64_t before = taken;
+        for (int w = 0; w < warp; ++w) before += s_scan[w];
         before += __popc(bal & ((1u << lane) - 1u));
         if (x < nb) kp[x] = (v > thr || (eq && before < rest)) ? 1 : 0;
         uint32_t chunk = 0;
-        for (int q = 0; q < kSelThreads / 32; ++q) chunk += s_scan[q];
+        for (int w = 0; w < kSelThreads / 32; ++w) chunk += s_scan[w];
         __syncthreads();
         taken += chunk;
     }
@@ -160,23 +237,57 @@ __global__ void __launch_bounds__(kThreads)
 
 }  // namespace
 
-size_t topk_workspace_bytes(uint32_t W, uint64_t n, uint32_t block) {
+// Workspace: norms [W][nb] float, keep [W][nb] bytes, the radix histograms
+// [4][W][256] and the per-slice equal counts [W][slices], each region
+// rounded to 256 bytes.
+namespace {
+struct TopkLayout {
+    uint64_t norms, keep, hist, eq, total, slices;
+};
+TopkLayout topk_layout(uint32_t W, uint64_t n, uint32_t block) {
     const uint64_t nb = (n + block - 1) / block;
-    const uint64_t norms = ((uint64_t)W * nb * 4 + 255) / 256 * 256;
-    return (size_t)(norms + ((uint64_t)W * nb + 255) / 256 * 256);
+    auto r256 = [](uint64_t x) { return (x + 255) / 256 * 256; };
+    TopkLayout L{};
+    L.slices = (nb + kSelSlice - 1) / kSelSlice;
+    L.norms = 0;
+    L.keep = r256((uint64_t)W * nb * 4);
+    L.hist = L.keep + r256((uint64_t)W * nb);
+    L.eq = L.hist + r256(4ull * W * 256 * 4);
+    L.total = L.eq + r256((uint64_t)W * L.slices * 4);
+    return L;
 }
+}  // namespace
+
+size_t topk_workspace_bytes(uint32_t W, uint64_t n, uint32_t block) { return (size_t)topk_layout(W, n, block).total; }
 
 cudaError_t launch_block_topk(const float* grad, float* resid, uint32_t W, uint64_t n, uint32_t block, uint64_t K,
                               float* sparse, void* workspace, cudaStream_t s) {
     const uint64_t nb = (n + block - 1) / block;
     if ((uint64_t)W * nb == 0) return cudaSuccess;
-    float* norms = static_cast<float*>(workspace);
-    uint8_t* keep = static_cast<uint8_t*>(workspace) + ((uint64_t)W * nb * 4 + 255) / 256 * 256;
+    const TopkLayout L = topk_layout(W, n, block);
+    char* ws = static_cast<char*>(workspace);
+    float* norms = reinterpret_cast<float*>(ws + L.norms);
+    uint8_t* keep = reinterpret_cast<uint8_t*>(ws + L.keep);
+    uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
+    uint32_t* eq = reinterpret_cast<uint32_t*>(ws + L.eq);
     const uint64_t blocks = ((uint64_t)W * nb + (kThreads / 32) - 1) / (kThreads / 32);
     topk_norms_kernel<<<grid_for(topk_norms_kernel, blocks), kThreads, 0, s>>>(grad, resid, n, block, nb, W, norms);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    topk_select_kernel<<<W, kSelThreads, 0, s>>>(norms, nb, K, keep);
+    const dim3 grid(W, (unsigned)L.slices);  // slices <= 65535: nb < 2^28 for n < 2^32
+    if (K > 0 && K < nb) {
+        e = launch_zero(reinterpret_cast<float*>(hist), 4ull * W * 256, s);
+        if (e != cudaSuccess) return e;
+        for (int pass = 0; pass < 4; ++pass) {
+            topk_hist_kernel<<<grid, kSelThreads, 0, s>>>(norms, nb, K, W, pass, hist);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
+        topk_eq_kernel<<<grid, kSelThreads, 0, s>>>(norms, nb, K, W, hist, eq);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    topk_keep_kernel<<<grid, kSelThreads, 0, s>>>(norms, nb, K, W, hist, eq, keep);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (n % 4 == 0)
