@@ -159,13 +159,15 @@ S2_API s2_status s2_encode_batched_blocks(const void *grad, s2_dtype dt, uint32_
  * the residual e_{t+1} = g_t - U(g_t) joins the next step's gradient).
  *   grad [W][n] float32 in; residual [W][n] float32 in/out (zeros at the
  *   first step); sparse_out [W][n] float32 out. Per worker: acc = grad +
- *   residual; the squared norm of every block of `block` elements (the last
- *   one may be shorter) is summed in float32 in a fixed order (lane l of 32
- *   accumulates fmaf(a, a, s) over elements l, l+32, ...; then an XOR
- *   butterfly over the 32 partials, offsets 16, 8, 4, 2, 1); the K blocks of
- *   largest norm are kept, ties going to the lower block index;
- *   sparse_out = acc on kept blocks and 0 elsewhere, residual = acc elsewhere
- *   and 0 on kept blocks.
+ *   residual (float32 additions); the K blocks of `block` elements (the last
+ *   one may be shorter) with the largest l2 norm are kept, ties going to the
+ *   lower block index; sparse_out = acc on kept blocks and 0 elsewhere,
+ *   residual = acc elsewhere and 0 on kept blocks.
+ *   The squared norms are summed in float32 in a fixed order, so the result
+ *   is deterministic; against the exact norms, each square passes through at
+ *   most ceil(block/32) + 5 roundings, and blocks whose exact norms differ by
+ *   less than that relative rounding may be ranked either way. Blocks with
+ *   identical contents always tie, and the lower index wins.
  *   block: a multiple of 32 (S2_ERR_UNSUPPORTED otherwise); K <= ceil(n/block)
  *   (S2_ERR_INVALID_ARG otherwise). workspace: s2_block_topk_workspace_size
  *   bytes, 16-byte aligned, contents on entry irrelevant.
@@ -287,7 +289,10 @@ S2_API s2_status s2_decode_compact(const uint32_t *bitmap, const float *sketch, 
  * returns S2_ERR_UNSUPPORTED beyond that.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) and caches it; make that first call before any
- *     stream capture.
+ *     stream capture. A lookup that fails (S2_ERR_CUDA) is not cached: the
+ *     next call on that device tries again. The cached address belongs to
+ *     the device's current context: after cudaDeviceReset on that device,
+ *     do not call this function again in the same process.
  *   - Every call on a device shares the one array: calls whose kernels can
  *     overlap on the GPU (different streams without ordering between them)
  *     race and corrupt each other's results. Order such calls, or use
@@ -330,18 +335,6 @@ S2_API s2_status s2_pipeline_workspace_size(s2_dtype dt, uint32_t W, uint64_t n,
 S2_API s2_status s2_pipeline_dense_host(const void *host_grad, s2_dtype dt, uint32_t W, uint64_t n,
                                  s2_params p, float scale, float *host_out, void *workspace,
                                  size_t workspace_bytes, s2_stream_t stream);
-
-/*
- * s2_take_device_fault -- read and clear this device's fault word.
- *   A kernel that waits on its own asynchronous copies must bound every wait
- *   and, if a wait gives up, record a nonzero code here and return early (the
- *   outputs of the calls since the last check are then not valid). No kernel
- *   of this version waits on anything, so the word stays 0; the call is kept
- *   so that callers can check it between steps. *fault_out receives the code
- *   (0 = no fault). Synchronises with the device (it reads device memory);
- *   call it between steps, not inside a hot loop.
- */
-S2_API s2_status s2_take_device_fault(uint32_t *fault_out);
 
 /* Human-readable name of a status code (static string). */
 S2_API const char *s2_status_string(s2_status st);

@@ -26,10 +26,11 @@ Parity status of each function (what pins it, in ``tests/test_oracle_pins.py``):
   encode_blocks /    block bitmap = numpy any() over each block; block size 1
   decode_dense_blocks  equals the element functions; exact recovery of every
                      position of marked blocks (zeros included) without collisions
-  block_topk         kept blocks = numpy's lexsort (norm desc, index asc) of the
-                     oracle's norms; norms within fp32 rounding of float64
-                     norms; sparse + residual = grad + residual exactly; the
-                     delta-approximate bound of Theorem 2 (K/nb of the energy)
+  block_topk /       norms = numpy's float64 norm of each block; kept blocks =
+  block_split        numpy's lexsort (norm desc, index asc) of those norms;
+                     a hand-worked four-block case; sparse + residual = grad +
+                     residual exactly; the delta-approximate bound of
+                     Theorem 2 (K/nb of the energy)
   sparse_list /      indices = numpy flatnonzero of the bit test, capacity keeps
   exact_sum          the true count; exact_sum = float64 numpy sum; equals the
                      S2 decode wherever no row collides
@@ -104,6 +105,8 @@ def _load():
         lib.s2o_exact_sum.restype = None
         lib.s2o_block_topk.argtypes = [vp, vp, u64, u64, u64, vp, vp, vp]
         lib.s2o_block_topk.restype = None
+        lib.s2o_block_split.argtypes = [vp, vp, u64, u64, vp, vp]
+        lib.s2o_block_split.restype = None
         _lib = lib
         return lib
 
@@ -271,17 +274,31 @@ def pipeline_blocks(grad: np.ndarray, block: int, d: int, w: int, seed: int, dty
 def block_topk(grad: np.ndarray, residual: np.ndarray, block: int, K: int):
     """Block-wise Top-K with error feedback for ONE worker (Section 2.2; Appendix A.2).
 
-    Returns (sparse float32[n], new residual float32[n], norms float32[nb], keep uint8[nb]).
+    Returns (sparse float32[n], new residual float32[n], squared block norms
+    float64[nb], keep uint8[nb]).
     """
     g = np.ascontiguousarray(grad, dtype=np.float32)
     e = np.array(residual, dtype=np.float32, copy=True)
     n = g.size
     nb = (n + block - 1) // block
     sp = np.empty(n, dtype=np.float32)
-    nrm = np.empty(max(nb, 1), dtype=np.float32)
+    nrm = np.empty(max(nb, 1), dtype=np.float64)
     keep = np.empty(max(nb, 1), dtype=np.uint8)
     _load().s2o_block_topk(_ptr(g), _ptr(e), n, block, K, _ptr(sp), _ptr(nrm), _ptr(keep))
     return sp, e, nrm[:nb], keep[:nb]
+
+
+def block_split(grad: np.ndarray, residual: np.ndarray, block: int, keep: np.ndarray):
+    """The error-feedback split of ONE worker for a given kept-block set
+    (Appendix A.2): returns (sparse float32[n], new residual float32[n])."""
+    g = np.ascontiguousarray(grad, dtype=np.float32)
+    e = np.array(residual, dtype=np.float32, copy=True)
+    n = g.size
+    kp = np.ascontiguousarray(keep, dtype=np.uint8)
+    assert kp.size == (n + block - 1) // block
+    sp = np.empty(n, dtype=np.float32)
+    _load().s2o_block_split(_ptr(g), _ptr(e), n, block, _ptr(kp if kp.size else np.zeros(1, np.uint8)), _ptr(sp))
+    return sp, e
 
 
 def sparse_list(grad: np.ndarray, capacity: Optional[int] = None):

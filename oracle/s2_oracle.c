@@ -341,58 +341,62 @@ void s2o_decode_dense_blocks(const uint32_t *bitmap, const double *S, const doub
 
 /* ---- block-wise Top-K sparsification with error feedback ------------------ */
 
-#include <math.h>
+/*
+ * Squared l2 norm of one block, as defined: the sum of the squares of its
+ * elements, accumulated in double precision in index order (each square of
+ * a float is exact in double). The pages fix no precision for the norm, so
+ * the plain definition is taken.
+ */
+static double block_norm2(const float *a, uint64_t len)
+{
+    double s = 0.0;
+    for (uint64_t j = 0; j < len; ++j)
+        s += (double)a[j] * (double)a[j];
+    return s;
+}
 
 /*
- * Squared l2 norm of one block in the order the path specifies (so that the
- * choice of blocks, an integer decision, is reproducible): 32 partial sums,
- * partial l accumulating fmaf(a, a, .) over the block's elements l, l+32,
- * l+64, ... in increasing order from 0.0f; then five butterfly steps, each
- * replacing every partial l by partial[l] + partial[l ^ off] for off = 16,
- * 8, 4, 2, 1. The result is partial[0].
+ * The split of the error-feedback step for one worker, given which blocks
+ * are kept ("S2 Reducer", Appendix A.2, proof of Theorem 2: U(g) is what is
+ * sent and e_{t+1} = g_t - U(g_t) is carried):
+ *   acc = grad + residual (one float addition per element);
+ *   sparse = acc on kept blocks, 0 elsewhere; residual = acc on the other
+ *   blocks, 0 on kept ones. keep: nb bytes, nonzero = kept.
  */
-static float block_norm2(const float *a, uint64_t len)
+void s2o_block_split(const float *grad, float *residual, uint64_t n, uint64_t block, const uint8_t *keep,
+                     float *sparse)
 {
-    float p[32];
-    for (int l = 0; l < 32; ++l) {
-        float s = 0.0f;
-        for (uint64_t j = (uint64_t)l; j < len; j += 32)
-            s = fmaf(a[j], a[j], s);
-        p[l] = s;
+    for (uint64_t i = 0; i < n; ++i) {
+        float acc = grad[i] + residual[i];
+        int kept = keep[i / block] != 0;
+        sparse[i] = kept ? acc : 0.0f;
+        residual[i] = kept ? 0.0f : acc;
     }
-    for (int off = 16; off >= 1; off >>= 1) {
-        float q[32];
-        for (int l = 0; l < 32; ++l)
-            q[l] = p[l] + p[l ^ off];
-        memcpy(p, q, sizeof(p));
-    }
-    return p[0];
 }
 
 /*
  * Block-wise Top-K with error feedback for one worker ("S2 Reducer", Section
- * 2.2 "Sparse Gradient & AllGather" for the sparsifier; Appendix A.2, proof of
- * Theorem 2, for the error sequence e_{t+1} = g_t - U(g_t)):
+ * 2.2 "Sparse Gradient & AllGather" for the sparsifier; Appendix A.2 for the
+ * error sequence):
  *   acc = grad + residual (float additions);
- *   view acc as blocks of `block` elements (the last one may be shorter),
- *   compute each block's squared l2 norm (block_norm2);
+ *   view acc as blocks of `block` elements (the last one may be shorter) and
+ *   take each block's squared l2 norm (block_norm2, double precision);
  *   keep the K blocks with the largest norms, ties to the lower block index;
- *   sparse = acc on kept blocks, 0 elsewhere; residual = acc - sparse
- *   (acc on the other blocks, 0 on kept ones).
- * norms (optional): nb floats. keep (optional): nb bytes, 1 for kept blocks.
+ *   split acc into the sent part and the new residual (s2o_block_split).
+ * norms (optional): nb doubles. keep (optional): nb bytes, 1 for kept blocks.
  */
 void s2o_block_topk(const float *grad, float *residual, uint64_t n, uint64_t block, uint64_t K, float *sparse,
-                    float *norms_out, uint8_t *keep_out)
+                    double *norms_out, uint8_t *keep_out)
 {
     uint64_t nb = (n + block - 1) / block;
-    float *acc = (float *)malloc((n ? n : 1) * sizeof(float));
-    float *nrm = (float *)malloc((nb ? nb : 1) * sizeof(float));
+    double *nrm = (double *)malloc((nb ? nb : 1) * sizeof(double));
     uint8_t *keep = (uint8_t *)calloc(nb ? nb : 1, 1);
-    for (uint64_t i = 0; i < n; ++i)
-        acc[i] = grad[i] + residual[i];
+    float *acc = (float *)malloc((block ? block : 1) * sizeof(float));
     for (uint64_t x = 0; x < nb; ++x) {
         uint64_t len = (x + 1) * block <= n ? block : n - x * block;
-        nrm[x] = block_norm2(acc + x * block, len);
+        for (uint64_t j = 0; j < len; ++j)
+            acc[j] = grad[x * block + j] + residual[x * block + j];
+        nrm[x] = block_norm2(acc, len);
     }
     /* K rounds of "largest remaining norm, lowest index among equals" */
     for (uint64_t r = 0; r < K && r < nb; ++r) {
@@ -402,13 +406,9 @@ void s2o_block_topk(const float *grad, float *residual, uint64_t n, uint64_t blo
                 best = x;
         keep[best] = 1;
     }
-    for (uint64_t i = 0; i < n; ++i) {
-        int kept = keep[i / block];
-        sparse[i] = kept ? acc[i] : 0.0f;
-        residual[i] = kept ? 0.0f : acc[i];
-    }
+    s2o_block_split(grad, residual, n, block, keep, sparse);
     if (norms_out)
-        memcpy(norms_out, nrm, nb * sizeof(float));
+        memcpy(norms_out, nrm, nb * sizeof(double));
     if (keep_out)
         memcpy(keep_out, keep, nb);
     free(acc);

@@ -45,7 +45,6 @@ __all__ = [
     "s2_pipeline_workspace_size",
     "s2_pipeline_dense_host",
     "s2_status_string",
-    "s2_take_device_fault",
     "s2_version",
     "S2_F32",
     "S2_BF16",
@@ -85,7 +84,6 @@ _SIGS = {
     "s2_hash": ([_vp, _u64, Params, _vp, _vp, _vp], _i32),
     "s2_pipeline_workspace_size": ([_i32, _u32, _u64, Params, ctypes.POINTER(_sz)], _i32),
     "s2_pipeline_dense_host": ([_vp, _i32, _u32, _u64, Params, _f32, _vp, _vp, _sz, _vp], _i32),
-    "s2_take_device_fault": ([ctypes.POINTER(_u32)], _i32),
     "s2_status_string": ([_i32], ctypes.c_char_p),
     "s2_version": ([], ctypes.c_char_p),
 }
@@ -131,13 +129,6 @@ def s2_status_string(status: int) -> str:
 
 def s2_version() -> str:
     return _f("s2_version")().decode()
-
-
-def s2_take_device_fault() -> int:
-    """Read and clear the device fault word (0 = every bounded wait completed)."""
-    v = _u32()
-    _check(_f("s2_take_device_fault")(ctypes.byref(v)), "s2_take_device_fault")
-    return int(v.value)
 
 
 def nwords(n: int) -> int:

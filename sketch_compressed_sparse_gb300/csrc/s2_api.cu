@@ -633,14 +633,6 @@ s2_status s2_pipeline_dense_host(const void* host_grad, s2_dtype dt, uint32_t W,
     return S2_OK;
 }
 
-s2_status s2_take_device_fault(uint32_t* fault_out) {
-    if (!fault_out) return S2_ERR_INVALID_ARG;
-    unsigned int v = 0;
-    if (take_encode_fault(&v) != cudaSuccess) return S2_ERR_CUDA;
-    *fault_out = v;
-    return S2_OK;
-}
-
 const char* s2_status_string(s2_status st) {
     switch (st) {
         case S2_OK: return "S2_OK";

@@ -418,22 +418,28 @@ static __device__ __align__(256) uint32_t
 uint64_t noalloc_compact_max_n() { return kNoAllocMaxN; }
 
 // Device address of the scratch for the current device. The address is looked
-// up once per device (cudaGetSymbolAddress with that device current) and
-// cached; host code must never pass the symbol itself to a kernel.
+// up with cudaGetSymbolAddress, with that device current, the first time a
+// call on the device succeeds in doing so, and cached from then on; a failed
+// lookup (for example one attempted during a stream capture) is not cached,
+// so the next call tries again. Host code must never pass the symbol itself
+// to a kernel: on the host it names a stand-in, not device memory.
 cudaError_t noalloc_compact_scratch(uint32_t** counts, uint32_t** offsets) {
-    static std::once_flag once[64];
+    static std::mutex mu;
     static uint32_t* base[64];
-    static cudaError_t status[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    std::call_once(once[dev], [dev] {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!base[dev]) {
         void* p = nullptr;
-        status[dev] = cudaGetSymbolAddress(&p, g_noalloc_compact_scratch);
+        e = cudaGetSymbolAddress(&p, g_noalloc_compact_scratch);
+        if (e != cudaSuccess) {
+            cudaGetLastError();  // leave no sticky launch error behind a failed lookup
+            return e;
+        }
         base[dev] = static_cast<uint32_t*>(p);
-    });
-    if (status[dev] != cudaSuccess) return status[dev];
+    }
     *counts = base[dev];
     *offsets = base[dev] + kNoAllocMaxTiles;
     return cudaSuccess;

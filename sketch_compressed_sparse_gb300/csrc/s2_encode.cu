@@ -572,10 +572,6 @@ __global__ void __launch_bounds__(kPrivThreads) encode_priv(EncodeArgs a, uint32
     }
 }
 
-// Fault word of s2_take_device_fault. No kernel of this library waits on
-// anything it could give up on, so nothing sets it; it stays 0.
-__device__ unsigned int g_fault = 0;
-
 // Zero `count` floats from any 4-byte-aligned address: a scalar head up to
 // the first 16-byte boundary, 16-byte stores, a scalar tail.
 __global__ void __launch_bounds__(kThreads) zero_f32(float* __restrict__ p, uint64_t count) {
@@ -737,14 +733,6 @@ cudaError_t launch_encode_smem(const EncodeArgs& a, int dtype, bool vec, bool on
         case 5: return launch_priv_d<5>(a, dtype, vec, only_if_preferred, launched, s);
         default: return launch_priv_d<0>(a, dtype, vec, only_if_preferred, launched, s);
     }
-}
-
-cudaError_t take_encode_fault(unsigned int* out) {
-    unsigned int v = 0, zero = 0;
-    cudaError_t e = cudaMemcpyFromSymbol(&v, g_fault, sizeof(v));
-    if (e == cudaSuccess && v) e = cudaMemcpyToSymbol(g_fault, &zero, sizeof(zero));
-    *out = v;
-    return e;
 }
 
 cudaError_t launch_zero(float* p, uint64_t count, cudaStream_t s) {

@@ -54,7 +54,6 @@ cudaError_t launch_zero(float* p, uint64_t count, cudaStream_t s);
 constexpr size_t kPrivMaxBytes = 192 * 1024;
 cudaError_t launch_encode_smem(const EncodeArgs& a, int dtype, bool vec, bool only_if_preferred, bool* launched,
                                cudaStream_t s);
-cudaError_t take_encode_fault(unsigned int* out);
 
 // ---- fused encode + reduce (single sketch) ----------------------------------
 struct FusedArgs {

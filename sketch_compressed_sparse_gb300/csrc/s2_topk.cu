@@ -4,13 +4,16 @@
 // carried into the next step's gradient).
 //
 // Per worker: acc = grad + residual; the squared norm of every block of
-// `block` elements in one fixed fp32 order (lane l of a warp accumulates
-// fmaf(a, a, s) over elements l, l+32, ... of the block, then a fixed XOR
-// butterfly), so that which blocks are kept -- an integer decision -- does
-// not depend on scheduling; the K-th largest norm by a 4-pass 8-bit radix
-// select over the norms' bit patterns (non-negative floats order like their
-// bits), ties broken towards the lower block index; finally sparse = acc on
-// kept blocks and residual = acc elsewhere.
+// `block` elements in float32, one warp per block (lane l accumulates
+// fmaf(a, a, s) over elements l, l+32, ... of the block, then an XOR
+// butterfly): a fixed order, so that which blocks are kept -- an integer
+// decision -- is the same on every run; the K-th largest norm by a 4-pass
+// 8-bit radix select over the norms' bit patterns (non-negative floats order
+// like their bits), ties broken towards the lower block index; finally
+// sparse = acc on kept blocks and residual = acc elsewhere. Against the
+// exact norm, each square passes through at most ceil(block/32) + 5
+// roundings, so blocks whose exact norms differ by less than that relative
+// rounding may be ranked either way.
 //
 // The select runs on many thread blocks per worker: each radix pass is one
 // launch that adds the digit counts of its slice of the norms into a global
@@ -154,6 +157,7 @@ __global__ void __launch_bounds__(kSelThreads)
     __shared__ uint32_t s_thr;
     __shared__ unsigned long long s_rest, s_base;
     __shared__ uint32_t s_scan[kSelThreads / 32];
+    __shared__ unsigned long long s_part[kSelThreads / 32];
     const uint32_t k = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint64_t x0 = (uint64_t)blockIdx.y * kSelSlice;
@@ -165,13 +169,20 @@ __global__ void __launch_bounds__(kSelThreads)
         }
         return;
     }
+    // equal norms in the slices before this one, summed by the whole block
+    unsigned long long part = 0;
+    for (uint32_t b = threadIdx.x; b < blockIdx.y; b += kSelThreads) part += eq_counts[(uint64_t)k * gridDim.y + b];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
+    if (lane == 0) s_part[warp] = part;
+    __syncthreads();
     if (threadIdx.x == 0) {
         uint32_t pm;
         uint64_t rest;
         select_state(hist, W, k, 4, K, &s_thr, &pm, &rest);
         s_rest = rest;
-        unsigned long long base = 0;  // equal norms in the slices before this one
-        for (uint32_t b = 0; b < blockIdx.y; ++b) base += eq_counts[(uint64_t)k * gridDim.y + b];
+        unsigned long long base = 0;
+        for (int w = 0; w < kSelThreads / 32; ++w) base += s_part[w];
         s_base = base;
     }
     __syncthreads();

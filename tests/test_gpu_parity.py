@@ -73,7 +73,6 @@ PIPELINE_CASES = [
 def test_pipeline_parity(name, kw):
     wl = workloads.tiny() if kw is None else workloads.custom(**kw)
     got = gpu_pipeline(_grad(wl), wl.d, wl.w, wl.seed, compact=True)
-    assert s2.s2_take_device_fault() == 0
     check_pipeline(wl.dense(), wl.dtype, got, wl.d, wl.w, wl.seed)
 
 

@@ -455,11 +455,9 @@ def test_block_topk_keeps_the_largest_blocks(n, block, K):
     sp, e2, nrm, keep = oracle.block_topk(g, e, block, K)
     acc = g + e  # float32 additions, as the method does
     nb = (n + block - 1) // block
-    ref = np.zeros(nb)
-    for x in range(nb):
-        ref[x] = np.sum(acc[x * block:(x + 1) * block].astype(np.float64) ** 2)
-    np.testing.assert_allclose(nrm, ref, rtol=1e-5)  # the specified fp32 order stays close to float64
-    order = np.lexsort((np.arange(nb), -nrm.astype(np.float64)))
+    ref = np.array([np.linalg.norm(acc[x * block:(x + 1) * block].astype(np.float64)) ** 2 for x in range(nb)])
+    np.testing.assert_allclose(nrm, ref, rtol=1e-13)  # the float64 norm, whatever the summation order
+    order = np.lexsort((np.arange(nb), -nrm))
     want = np.zeros(nb, dtype=np.uint8)
     want[order[:K]] = 1
     np.testing.assert_array_equal(keep, want)
@@ -467,6 +465,29 @@ def test_block_topk_keeps_the_largest_blocks(n, block, K):
     np.testing.assert_array_equal(sp, np.where(kept, acc, 0).astype(np.float32))
     np.testing.assert_array_equal(sp + e2, acc)  # residual carries exactly what was not sent
     assert (e2[kept] == 0).all()
+    sp3, e3 = oracle.block_split(g, e, block, keep)  # the split alone, given the same kept blocks
+    np.testing.assert_array_equal(sp3.view(np.uint32), sp.view(np.uint32))
+    np.testing.assert_array_equal(e3.view(np.uint32), e2.view(np.uint32))
+
+
+def test_block_topk_worked_four_block_case():
+    # Blocks of two elements, worked by hand (squared norms of grad + residual):
+    #   block 0: [3, -4]            -> 25
+    #   block 1: [0, -5]            -> 25
+    #   block 2: [4.9, 0] + [0, 1.5] -> 24.01 + 2.25 = 26.26
+    #   block 3: [-1, -4.95]        -> 1 + 24.5025 = 25.5025
+    # K = 2 keeps blocks 2 and 3; K = 3 adds block 0 (25 = 25, lower index).
+    # Ranking by the signed sum, |sum|, max |x|, the gradient without the
+    # residual, or ties to the higher index would keep another set.
+    g = np.array([3, -4, 0, -5, 4.9, 0, -1, -4.95], dtype=np.float32)
+    e = np.array([0, 0, 0, 0, 0, 1.5, 0, 0], dtype=np.float32)
+    _, _, nrm, keep = oracle.block_topk(g, e, 2, 2)
+    np.testing.assert_allclose(nrm, [25.0, 25.0, 26.26, 25.5025], rtol=1e-6)
+    np.testing.assert_array_equal(keep, [0, 0, 1, 1])
+    sp, e2, _, keep3 = oracle.block_topk(g, e, 2, 3)
+    np.testing.assert_array_equal(keep3, [1, 0, 1, 1])
+    np.testing.assert_array_equal(sp, np.array([3, -4, 0, 0, 4.9, 1.5, -1, -4.95], dtype=np.float32))
+    np.testing.assert_array_equal(e2, np.array([0, 0, 0, -5, 0, 0, 0, 0], dtype=np.float32))
 
 
 def test_block_topk_ties_go_to_the_lower_block():
