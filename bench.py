@@ -6,9 +6,13 @@ path over one batch of synthetic input, with the inputs already in HBM.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
 
-Prints ONE JSON line (rank 0). ``value`` is W*n gradient elements per second
-(Gelem/s) over the K timed steps, whole job. L2 is flushed (a 512 MiB write)
-before every step, outside the timed events. ``roofline`` is the dominant
+Prints ONE JSON line (rank 0). The default workload is the largest one, the
+large-LM embedding table (267,735 x 1024 fp32, W=4, d=5, w=2^22); the line's
+``per_config`` object carries the same measurements for the embedding
+(33,278 x 512) and top-k (ResNet-50 size) workloads, timed in the same run.
+``value`` is W*n gradient elements per second (Gelem/s) over the K timed
+steps, whole job. L2 is flushed (a 512 MiB write) before every step, outside
+the timed events. ``roofline`` is the dominant
 kernel (encode) against the measured HBM copy bandwidth; ``path_roofline`` the
 whole step. ``e2e`` times the same path from pinned host memory to host memory
 through the C-ABI call s2_pipeline_dense_host. ``cpu_baseline`` times the CPU
@@ -295,7 +299,7 @@ def time_oracle_threads(wl: workloads.Workload, G: np.ndarray) -> dict:
 
 # ---------------------------------------------------------------- our arm
 
-def run_ours(args, wl, world, rank, local):
+def run_ours(args, wl, world, rank, local, config_name=None):
     import torch
 
     import sketch_compressed_sparse_gb300 as s2
@@ -403,7 +407,7 @@ def run_ours(args, wl, world, rank, local):
     n_dec = 3 if args.decode == "compact" else dense_decode_launches(n, l2)
     ach_enc = by["encode"] / enc_s / 1e9
     path_gbs = by["total"] / (total_ms / 1e3 / K) / 1e9
-    traffic = recorded_traffic(args.config)
+    traffic = recorded_traffic(config_name or args.config)
 
     res = {
         "metric": METRIC,
@@ -484,6 +488,28 @@ def run_ours(args, wl, world, rank, local):
             "sample": f"the same pass with the {wl.W} workers' encodes on {ot['threads']} host threads, reduce and "
                       f"decode on one ({ot['seconds']:.2f} s; host has {os.cpu_count()} cores)"}
     return res
+
+
+# The workloads whose whole-path HBM fraction is a target, besides the headline.
+GATED_CONFIGS = ("embedding", "topk")
+PER_CONFIG_KEYS = ("value", "unit", "ms_per_step", "steps", "warmup", "config", "stages_ms_per_step", "roofline",
+                   "path_roofline", "l2_roofline", "gpu_launches", "clocks", "e2e", "cpu_baseline",
+                   "cpu_baseline_threads")
+
+
+def run_per_config(args, world, rank, local, names=GATED_CONFIGS) -> dict:
+    """The same measurement on the other gated workloads, one after the other
+    in this process (each with its own warm-up and timed steps)."""
+    import torch
+
+    out = {}
+    for name in names:
+        wl = workloads.by_name(name)
+        r = run_ours(args, wl, world, rank, local, config_name=name)
+        out[r["config"]["workload"]] = {k: r[k] for k in PER_CONFIG_KEYS if k in r}
+        del wl, r
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_blocktopk(args, world, rank, local):
@@ -847,8 +873,10 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="embedding",
+    ap.add_argument("--config", default="large_lm",
                     choices=["tiny", "embedding", "topk", "large_lm", "blocktopk", "sweep"])
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="large_lm per-worker run only: skip the embedding and top-k measurements in per_config")
     ap.add_argument("--sweep-max-log2", type=int, default=28,
                     help="--config sweep: largest gradient length as a power of two (20..28)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
@@ -907,6 +935,12 @@ def main(argv=None):
             res = run_allgather(args, workloads.by_name(args.config), world, rank, local)
         else:
             res = run_ours(args, select_workers(workloads.by_name(args.config), args.workers), world, rank, local)
+            if (args.config == "large_lm" and args.mode == "per_worker" and args.workers is None
+                    and not args.no_per_config):
+                import torch
+
+                torch.cuda.empty_cache()
+                res["per_config"] = run_per_config(args, world, rank, local)
         if world > 1:
             import torch.distributed as dist
 
