@@ -138,8 +138,16 @@ def encode_launches(wl: workloads.Workload, l2_bytes: int, sms: int = 152) -> in
     return 2 * ((wl.W + group - 1) // group)
 
 
-def dense_decode_launches(n: int, l2_bytes: int) -> int:
-    """A dense output larger than L2 is written in two launches (zeros first)."""
+def dense_decode_launches(n: int, l2_bytes: int, d: int = 0, w: int = 0, block: int = 0) -> int:
+    """Launches of one s2_decode_dense_ws call: a summed sketch larger than a
+    third of L2 (d = 3 or 5, element bitmap) is decoded by a zero launch and
+    one launch per group of rows that fits in a third of L2; otherwise a dense
+    output larger than L2 is written in two launches (zeros first), a smaller
+    one in one."""
+    budget = l2_bytes // 3
+    if not block and d in (3, 5) and 4 * d * w > budget:
+        rpp = 1 if 4 * w >= budget else budget // (4 * w)
+        return 1 + -(-d // rpp)
     return 2 if 4 * n > l2_bytes else 1
 
 
@@ -156,7 +164,7 @@ def kernel_source_sha() -> str:
     """Hash of the sources that define the encode stage (its kernels and their helpers)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sketch_compressed_sparse_gb300", "csrc")
-    for f in ("s2_device.cuh", "s2_internal.h", "s2_encode.cu"):
+    for f in ("s2_device.cuh", "s2_internal.h", "s2_tasks.cuh", "s2_encode.cu"):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -318,6 +326,7 @@ def run_ours(args, wl, world, rank, local, config_name=None):
     else:
         bitmaps = torch.empty((W, s2.nwords(nbits)), dtype=torch.int32, device=dev)
         sketches = torch.empty((W, d, w), dtype=torch.float32, device=dev)
+
     bitmap = torch.empty(s2.nwords(nbits), dtype=torch.int32, device=dev)
     sketch = torch.empty((d, w), dtype=torch.float32, device=dev)
     compact = args.decode == "compact"
@@ -331,6 +340,7 @@ def run_ours(args, wl, world, rank, local, config_name=None):
         out = None
     else:
         out = torch.empty(n, dtype=torch.float32, device=dev)
+        dws = torch.empty(max(s2.s2_decode_dense_workspace_size(n, d, w), 1), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -348,7 +358,7 @@ def run_ours(args, wl, world, rank, local, config_name=None):
         elif compact:
             s2.s2_decode_compact(bitmap, sketch, n, d, w, seed, cidx, cval, ccnt, cws)
         else:
-            s2.s2_decode_dense(bitmap, sketch, n, d, w, seed, out)
+            s2.s2_decode_dense_ws(bitmap, sketch, n, d, w, seed, out, dws)
 
     def step():
         if fused:
@@ -404,7 +414,7 @@ def run_ours(args, wl, world, rank, local, config_name=None):
     peak = peaks["hbm_gbs"]
     enc_s = enc_ms / 1e3 / K
     n_enc = encode_launches(wl, l2)
-    n_dec = 3 if args.decode == "compact" else dense_decode_launches(n, l2)
+    n_dec = 3 if args.decode == "compact" else dense_decode_launches(n, l2, d, w, blk)
     ach_enc = by["encode"] / enc_s / 1e9
     path_gbs = by["total"] / (total_ms / 1e3 / K) / 1e9
     traffic = recorded_traffic(config_name or args.config)
@@ -448,7 +458,7 @@ def run_ours(args, wl, world, rank, local, config_name=None):
                   peak_source="scattered red.f32 rate measured by bench.py --ceilings (profiles/ceilings_gb300.json)")
     res["l2_roofline"] = l2
     res["config"]["mode"] = ("per_worker (encode_batched + reduce + decode_compact)" if compact else
-                             "per_worker (encode_batched + reduce + decode_dense)")
+                             "per_worker (encode_batched + reduce + decode_dense_ws)")
     if blk:
         res["config"]["mode"] = f"per_worker, block bitmap of {blk} positions (encode_batched_blocks + reduce + decode_dense_blocks)"
         res["gpu_launches"] = K * (n_enc + 1 + 1 + n_dec)  # + the block bitmaps' zero fill
@@ -458,7 +468,7 @@ def run_ours(args, wl, world, rank, local, config_name=None):
         fused_s = enc_ms / 1e3 / K
         ach = byf["encode_reduce_fused"] / fused_s / 1e9
         pg = byf["total"] / step_s / 1e9
-        res["config"]["mode"] = "fused_single_sketch (encode_reduce_fused + decode_dense)"
+        res["config"]["mode"] = "fused_single_sketch (encode_reduce_fused + decode_dense_ws)"
         res["stages_ms_per_step"] = {"encode_reduce_fused": round(enc_ms / K, 5), "decode": round(dec_ms / K, 5)}
         res["roofline"] = {"kernel": "encode_reduce_fused (zero fill + one pass over all workers)", "bound": "hbm",
                            "achieved": round(ach, 1), "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),

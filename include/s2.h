@@ -251,6 +251,33 @@ S2_API s2_status s2_decode_dense_blocks(const uint32_t *block_bitmap, const floa
                                         uint32_t block, s2_params p, float scale, float *out,
                                         s2_stream_t stream);
 
+/*
+ * s2_decode_dense_ws -- s2_decode_dense with a workspace, for summed sketches
+ * too large to stay in the L2 cache under random reads (Section 3.1
+ * "Decompressing Sparse Gradient"; the median query of Algorithm 1).
+ *   Arguments, results and errors as s2_decode_dense, plus
+ *   workspace: device scratch of at least s2_decode_dense_workspace_size(n, p)
+ *   bytes (about 8n for d = 5 and 4n for d = 3, plus 4 bytes per 512
+ *   positions; 0 for other d), 16-byte aligned, not overlapping the other
+ *   arrays; its contents on entry do not matter (S2_ERR_INVALID_ARG if it is
+ *   too small).
+ * When the sketch (4*d*w bytes) is larger than a third of this device's L2
+ * cache and d is 3 or 5, the median is taken in passes over groups of whole
+ * rows that fit in a third of L2: a first launch writes the zeros of every
+ * 512-position stretch without a set bit and lists the others; each pass then
+ * reads only its rows for every set position of the listed stretches and
+ * carries the candidates for the median that remain (at most 2 for d = 3, 3
+ * for d = 5) to the next pass in `out` and the workspace. The
+ * decoded values are the same as s2_decode_dense's (the median selects one
+ * of the row values, or averages none); an estimate of zero may come out as
+ * +0.0 or -0.0 as with s2_decode_dense. Otherwise the call launches exactly
+ * what s2_decode_dense launches and does not touch the workspace.
+ */
+S2_API s2_status s2_decode_dense_workspace_size(uint64_t n, s2_params p, size_t *bytes);
+S2_API s2_status s2_decode_dense_ws(const uint32_t *bitmap, const float *sketch, uint64_t n, s2_params p,
+                                    float scale, float *out, void *workspace, size_t workspace_bytes,
+                                    s2_stream_t stream);
+
 /* Device workspace bytes that s2_decode_compact needs for length n. */
 S2_API s2_status s2_decode_workspace_size(uint64_t n, size_t *bytes);
 

@@ -39,6 +39,8 @@ __all__ = [
     "s2_decode_dense_blocks",
     "s2_decode_dense",
     "s2_decode_workspace_size",
+    "s2_decode_dense_workspace_size",
+    "s2_decode_dense_ws",
     "s2_decode_compact",
     "s2_decode_compact_noalloc",
     "s2_hash",
@@ -68,6 +70,7 @@ _SIGS = {
     "s2_encode": ([_vp, _i32, _u64, Params, _vp, _vp, _vp], _i32),
     "s2_encode_batched": ([_vp, _i32, _u32, _u64, Params, _vp, _vp, _vp], _i32),
     "s2_encode_batched_path": ([_vp, _i32, _u32, _u64, Params, _i32, _vp, _vp, _vp], _i32),
+
     "s2_reduce": ([_vp, _vp, _u32, _u64, Params, _vp, _vp, _vp], _i32),
     "s2_encode_reduce_fused": ([_vp, _i32, _u32, _u64, Params, _vp, _vp, _vp], _i32),
     "s2_encode_batched_blocks": ([_vp, _i32, _u32, _u64, _u32, Params, _vp, _vp, _vp], _i32),
@@ -79,6 +82,8 @@ _SIGS = {
     "s2_decode_dense_blocks": ([_vp, _vp, _u64, _u32, Params, _f32, _vp, _vp], _i32),
     "s2_decode_dense": ([_vp, _vp, _u64, Params, _f32, _vp, _vp], _i32),
     "s2_decode_workspace_size": ([_u64, ctypes.POINTER(_sz)], _i32),
+    "s2_decode_dense_workspace_size": ([_u64, Params, ctypes.POINTER(_sz)], _i32),
+    "s2_decode_dense_ws": ([_vp, _vp, _u64, Params, _f32, _vp, _vp, _sz, _vp], _i32),
     "s2_decode_compact": ([_vp, _vp, _u64, Params, _f32, _vp, _vp, _u64, _vp, _vp, _sz, _vp], _i32),
     "s2_decode_compact_noalloc": ([_vp, _vp, _u64, Params, _f32, _vp, _vp, _u64, _vp, _vp], _i32),
     "s2_hash": ([_vp, _u64, Params, _vp, _vp, _vp], _i32),
@@ -309,6 +314,21 @@ def s2_decode_dense(bitmap: torch.Tensor, sketch: torch.Tensor, n: int, d: int, 
            "s2_decode_dense")
 
 
+def s2_decode_dense_workspace_size(n: int, d: int, w: int) -> int:
+    b = _sz()
+    _check(_f("s2_decode_dense_workspace_size")(n, Params(d, w, 0), ctypes.byref(b)), "s2_decode_dense_workspace_size")
+    return int(b.value)
+
+
+def s2_decode_dense_ws(bitmap: torch.Tensor, sketch: torch.Tensor, n: int, d: int, w: int, seed: int,
+                       out: torch.Tensor, workspace: torch.Tensor, scale: float = 1.0, stream=None) -> None:
+    """s2_decode_dense with a workspace (the row-pass median for sketches larger than L2 can hold)."""
+    _check(_f("s2_decode_dense_ws")(_dev(bitmap, "bitmap", _U32, nwords(n)), _dev(sketch, "sketch", (torch.float32,), d * w),
+                                    n, Params(d, w, seed), scale, _dev(out, "out", (torch.float32,), n),
+                                    _dev(workspace, "workspace", (torch.uint8,)), workspace.numel(), _stream(stream)),
+           "s2_decode_dense_ws")
+
+
 def s2_decode_workspace_size(n: int) -> int:
     b = _sz()
     _check(_f("s2_decode_workspace_size")(n, ctypes.byref(b)), "s2_decode_workspace_size")
@@ -377,3 +397,4 @@ def s2_pipeline_dense_host(host_grad: torch.Tensor, d: int, w: int, seed: int, h
 def alloc_encode_outputs(W: int, n: int, d: int, w: int, device="cuda") -> Tuple[torch.Tensor, torch.Tensor]:
     return (torch.empty((W, nwords(n)), dtype=torch.int32, device=device),
             torch.empty((W, d, w), dtype=torch.float32, device=device))
+

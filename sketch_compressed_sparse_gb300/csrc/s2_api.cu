@@ -274,7 +274,7 @@ const void* mapped_host(const void* p) {
 }
 
 struct PipelineLayout {
-    size_t grad, bitmaps, sketches, bitmap, sketch, out, total;
+    size_t grad, bitmaps, sketches, bitmap, sketch, out, dec_ws, total;
 };
 
 PipelineLayout pipeline_layout(s2_dtype dt, uint32_t W, uint64_t n, s2_params p) {
@@ -293,6 +293,8 @@ PipelineLayout pipeline_layout(s2_dtype dt, uint32_t W, uint64_t n, s2_params p)
     off += round256((size_t)dw * 4);
     L.out = off;
     off += round256((size_t)n * 4);
+    L.dec_ws = off;
+    off += round256(dense_workspace_bytes(n, p.d));
     L.total = off;
     return L;
 }
@@ -480,6 +482,30 @@ s2_status s2_decode_dense(const uint32_t* bitmap, const float* sketch, uint64_t 
         launch_decode_dense(make_decode_args(bitmap, sketch, n, p, scale), out, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+s2_status s2_decode_dense_workspace_size(uint64_t n, s2_params p, size_t* bytes) {
+    if (!bytes) return S2_ERR_INVALID_ARG;
+    s2_status st = check_params(p);
+    if (st != S2_OK) return st;
+    if (n > kMaxN) return S2_ERR_UNSUPPORTED;
+    *bytes = dense_workspace_bytes(n, p.d);
+    return S2_OK;
+}
+
+s2_status s2_decode_dense_ws(const uint32_t* bitmap, const float* sketch, uint64_t n, s2_params p, float scale,
+                             float* out, void* workspace, size_t workspace_bytes, s2_stream_t stream) {
+    s2_status st = check_decode_dense(bitmap, sketch, n, p, out);
+    if (st != S2_OK || n == 0) return st;
+    const size_t need = dense_workspace_bytes(n, p.d);
+    if (workspace_bytes < need || (need > 0 && !workspace)) return S2_ERR_INVALID_ARG;
+    if (!aligned(workspace, 16)) return S2_ERR_ALIGNMENT;
+    const uint64_t dw = (uint64_t)p.d * p.w;
+    if (overlap(workspace, need, out, n * 4) || overlap(workspace, need, bitmap, words_of(n) * 4) ||
+        overlap(workspace, need, sketch, dw * 4))
+        return S2_ERR_INVALID_ARG;
+    return cuda_status(launch_decode_dense_ws(make_decode_args(bitmap, sketch, n, p, scale), out,
+                                              static_cast<float*>(workspace), reinterpret_cast<cudaStream_t>(stream)));
+}
+
 s2_status s2_decode_workspace_size(uint64_t n, size_t* bytes) {
     if (!bytes) return S2_ERR_INVALID_ARG;
     if (n > kMaxN) return S2_ERR_UNSUPPORTED;
@@ -625,7 +651,8 @@ s2_status s2_pipeline_dense_host(const void* host_grad, s2_dtype dt, uint32_t W,
     if (st != S2_OK) return st;
     if (n == 0) return S2_OK;
     float* out_mapped = static_cast<float*>(const_cast<void*>(mapped_host(host_out)));
-    st = s2_decode_dense(d_bitmap, d_sketch, n, p, scale, out_mapped ? out_mapped : d_out, stream);
+    st = s2_decode_dense_ws(d_bitmap, d_sketch, n, p, scale, out_mapped ? out_mapped : d_out, ws + L.dec_ws,
+                            dense_workspace_bytes(n, p.d), stream);
     if (st != S2_OK) return st;
     if (!out_mapped &&
         cudaMemcpyAsync(host_out, d_out, (size_t)n * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)

@@ -167,6 +167,187 @@ __global__ void __launch_bounds__(kThreads) decode_dense_kernel(DecodeArgs a, fl
     }
 }
 
+// ---- dense decode in passes over groups of rows -------------------------------
+// A summed sketch much larger than a third of L2 does not stay in L2 under
+// random gathers (84 MB of large-LM sketch: 44 % hits), so the median is
+// taken in passes: each pass gathers only its group of rows, which L2 holds,
+// for every set position, and carries to the next pass the candidates of the
+// median that remain after the rows seen so far. Of 3 rows at most 2
+// candidates remain (after 2 rows: their min and max); of 5 rows at most 3
+// (after 2 rows: min and max; after 3: all three, sorted; after 4: the middle
+// two of the four, since the smallest and the largest of four cannot be the
+// third of five). The candidates live at the position's own index in the
+// output (the first) and in up to two workspace arrays of n floats, so each
+// pass reads and writes them with coalesced 16-byte accesses. Tasks without
+// a set position are written (zeros) by one launch before the passes, which
+// skip them; the last pass writes every position of the other tasks.
+
+// Median candidates left after r of D rows.
+__host__ __device__ constexpr int kept_after(int D, int r) {
+    return D == 3 ? (r == 0 ? 0 : (r == 1 ? 1 : (r == 2 ? 2 : 1)))
+                  : (r == 0 ? 0 : (r == 1 ? 1 : (r == 2 ? 2 : (r == 3 ? 3 : (r == 4 ? 2 : 1)))));
+}
+
+// Fold the value e of row r (rows counted from 0) into the candidates c.
+template <int D>
+__device__ __forceinline__ void fold_row(float (&c)[3], int r, float e) {
+    if (r == 0) {
+        c[0] = e;
+    } else if (r == 1) {
+        const float lo = fminf(c[0], e), hi = fmaxf(c[0], e);
+        c[0] = lo;
+        c[1] = hi;
+    } else if (D == 3 || r == 4) {  // the median: of lo <= hi and e
+        c[0] = fmaxf(c[0], fminf(c[1], e));
+    } else if (r == 2) {  // three sorted values
+        const float x = fminf(c[0], e), y = fmaxf(c[0], fminf(c[1], e)), z = fmaxf(c[1], e);
+        c[0] = x;
+        c[1] = y;
+        c[2] = z;
+    } else {  // r == 3: the middle two of four
+        const float p = fmaxf(c[0], fminf(c[1], e)), q = fminf(c[2], fmaxf(c[1], e));
+        c[0] = p;
+        c[1] = q;
+    }
+}
+
+// Four consecutive floats at e (16-byte aligned when e + 4 <= n), streamed.
+__device__ __forceinline__ float4 ld_stream_f4_tail(const float* p, uint64_t e, uint64_t n) {
+    if (e + 4 <= n) {
+        const uint4 v = ld_stream_u4(p + e);
+        return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
+    }
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (e + 0 < n) v.x = ld_stream_f32(p + e + 0);
+    if (e + 1 < n) v.y = ld_stream_f32(p + e + 1);
+    if (e + 2 < n) v.z = ld_stream_f32(p + e + 2);
+    return v;
+}
+
+__device__ __forceinline__ void st_stream_f4_tail(float* p, uint64_t e, uint64_t n, float4 v) {
+    if (e + 4 <= n) {
+        st_stream_f4(p + e, v);
+    } else {
+        if (e + 0 < n) p[e + 0] = v.x;
+        if (e + 1 < n) p[e + 1] = v.y;
+        if (e + 2 < n) p[e + 2] = v.z;
+    }
+}
+
+__device__ __forceinline__ float f4_at(const float4& v, int q) {
+    return q == 0 ? v.x : (q == 1 ? v.y : (q == 2 ? v.z : v.w));
+}
+
+// Bitmap word wi of a task, read once per pass (evict-first), bits >= n cleared.
+__device__ __forceinline__ uint32_t task_word(const DecodeArgs& a, uint64_t wi, int lane) {
+    uint32_t v = 0;
+    if (lane < kTaskWords && wi < a.nw) {
+        v = ld_stream_u32(a.bitmap + wi);
+        if (wi == a.nw - 1 && (a.n & 31)) v &= (1u << (a.n & 31)) - 1u;
+    }
+    return v;
+}
+
+// The launch before the passes: writes the 512 zeros of every task without a
+// set position and lists the others (task ids in any order, their number in
+// *count, which starts at zero) for the passes to work through.
+__global__ void __launch_bounds__(kThreads)
+    decode_zero_list_kernel(DecodeArgs a, float* __restrict__ out, uint32_t* __restrict__ list,
+                            unsigned int* __restrict__ count) {
+    const int lane = threadIdx.x & 31;
+    const uint64_t ntasks = (a.n + kTaskElems - 1) / kTaskElems;
+    const uint64_t nwarps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
+    for (uint64_t t = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < ntasks; t += nwarps) {
+        const uint32_t mask = lane_mask(task_word(a, t * kTaskWords + lane, lane), lane);
+        if (__any_sync(kFull, mask != 0)) {
+            if (lane == 0) list[atomicAdd(count, 1u)] = (uint32_t)t;
+            continue;
+        }
+        const uint64_t e0 = t * kTaskElems;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) st_stream_f4_tail(out, e0 + u * 128 + lane * 4, a.n, make_float4(0.f, 0.f, 0.f, 0.f));
+    }
+}
+
+// One pass over rows [j0, j1) of the median (D = 3 or 5), one warp per listed
+// task of 512 positions; a lane owns 4 chunks of 4 consecutive positions,
+// like decode_dense_kernel.
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+    decode_rows_kernel(DecodeArgs a, float* __restrict__ out, float* __restrict__ cand1,
+                       float* __restrict__ cand2, const uint32_t* __restrict__ list,
+                       const unsigned int* __restrict__ count, int j0, int j1) {
+    static_assert(D == 3 || D == 5, "row passes are specialised for 3 and 5 rows");
+    __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
+    load_keys(a.keys, s_kh, s_ks);
+    const int lane = threadIdx.x & 31;
+    const uint64_t keep = policy_evict_last();
+    const int k_in = kept_after(D, j0), k_out = kept_after(D, j1);
+    const bool last = j1 == D;
+    const uint32_t listed = *count;
+    const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+    for (uint32_t x = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; x < listed; x += nwarps) {
+        const uint64_t t = list[x];
+        const uint64_t e0 = t * kTaskElems;
+        const uint32_t mask = lane_mask(task_word(a, t * kTaskWords + lane, lane), lane);
+#pragma unroll 1
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t nib = (mask >> (4 * u)) & 0xfu;
+            const uint64_t e = e0 + u * 128 + lane * 4;
+            if (!nib && !last) continue;
+            float c[4][3] = {};
+            if (nib) {
+                if (k_in >= 1) {
+                    const float4 v = ld_stream_f4_tail(out, e, a.n);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) c[q][0] = f4_at(v, q);
+                }
+                if (k_in >= 2) {
+                    const float4 v = ld_stream_f4_tail(cand1, e, a.n);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) c[q][1] = f4_at(v, q);
+                }
+                if (k_in >= 3) {
+                    const float4 v = ld_stream_f4_tail(cand2, e, a.n);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) c[q][2] = f4_at(v, q);
+                }
+                // every gather of the pass first, then the folds
+                float ev[4][D];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t i = (uint32_t)(e + q);
+#pragma unroll
+                    for (int j = 0; j < D; ++j) {
+                        ev[q][j] = 0.f;
+                        if (j >= j0 && j < j1 && ((nib >> q) & 1u)) {
+                            const uint32_t b = bucket_of(i, s_kh[j], a.w);
+                            ev[q][j] = apply_sign(ld_gather_f32(a.sketch + (uint64_t)j * a.w + b, keep),
+                                                  signbit_of(i, s_ks[j]));
+                        }
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                    for (int j = 0; j < D; ++j)
+                        if (j >= j0 && j < j1) fold_row<D>(c[q], j, ev[q][j]);
+                }
+            }
+            if (last) {
+                float r[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) r[q] = ((nib >> q) & 1u) ? a.scale * c[q][0] : 0.f;
+                st_stream_f4_tail(out, e, a.n, make_float4(r[0], r[1], r[2], r[3]));
+            } else {
+                st_stream_f4_tail(out, e, a.n, make_float4(c[0][0], c[1][0], c[2][0], c[3][0]));
+                if (k_out >= 2) st_stream_f4_tail(cand1, e, a.n, make_float4(c[0][1], c[1][1], c[2][1], c[3][1]));
+                if (k_out >= 3) st_stream_f4_tail(cand2, e, a.n, make_float4(c[0][2], c[1][2], c[2][2], c[3][2]));
+            }
+        }
+    }
+}
+
 // ---- compacted output -------------------------------------------------------
 
 // Set bits per tile of kCompactTileWords words (one word per thread), and the
@@ -338,6 +519,38 @@ cudaError_t launch_dense_d(const DecodeArgs& a, float* out, cudaStream_t s) {
     return a.block ? launch_dense_db<D, true>(a, out, s) : launch_dense_db<D, false>(a, out, s);
 }
 
+// Rows of the summed sketch that one pass of the sliced dense decode gathers
+// from: as many whole rows as fit in a third of L2 (at least one).
+uint32_t rows_per_pass(uint64_t w, uint64_t l2_bytes) {
+    const uint64_t budget = l2_bytes / 3, row = 4 * w;
+    return row >= budget ? 1u : (uint32_t)(budget / row);
+}
+
+template <int D>
+cudaError_t launch_dense_rows(const DecodeArgs& a, float* out, float* ws, uint32_t rpp, cudaStream_t s) {
+    const uint64_t tasks = (a.n + kTaskElems - 1) / kTaskElems;
+    const uint64_t blocks = (tasks + (kThreads / 32) - 1) / (kThreads / 32);
+    const DenseWsLayout L = dense_ws_layout(a.n, a.d);
+    float* cand1 = ws + L.cand1 / 4;
+    float* cand2 = ws + L.cand2 / 4;
+    unsigned int* count = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(ws) + L.count);
+    uint32_t* list = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(ws) + L.list);
+    cudaError_t e = cudaMemsetAsync(count, 0, sizeof(unsigned int), s);
+    if (e != cudaSuccess) return e;
+    // zeros of the tasks without a set position; the list of the others
+    decode_zero_list_kernel<<<grid_for(decode_zero_list_kernel, blocks), kThreads, 0, s>>>(a, out, list, count);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int grid = grid_for(decode_rows_kernel<D>, blocks);
+    for (uint32_t j0 = 0; j0 < (uint32_t)D; j0 += rpp) {
+        const uint32_t j1 = j0 + rpp < (uint32_t)D ? j0 + rpp : (uint32_t)D;
+        decode_rows_kernel<D><<<grid, kThreads, 0, s>>>(a, out, cand1, cand2, list, count, (int)j0, (int)j1);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 template <int D>
 cudaError_t launch_compact_write_d(const DecodeArgs& a, const uint32_t* tile_counts, const uint32_t* offsets,
                                    const uint16_t* task_prefix, uint32_t* idx_out, float* val_out,
@@ -359,6 +572,40 @@ cudaError_t launch_decode_dense(const DecodeArgs& a, float* out, cudaStream_t s)
         case 1: return launch_dense_d<1>(a, out, s);
         default: return launch_dense_d<0>(a, out, s);
     }
+}
+
+// Workspace of the row-pass dense decode: the candidate arrays (n floats
+// each, rounded to 64), the listed-task count (256 bytes), the task list
+// (one 32-bit id per task of 512 positions). Empty for other d.
+DenseWsLayout dense_ws_layout(uint64_t n, uint32_t d) {
+    DenseWsLayout L{};
+    if (d != 3 && d != 5) return L;
+    const uint64_t arr = (n + 63) / 64 * 64 * 4;
+    const uint64_t tasks = (n + kTaskElems - 1) / kTaskElems;
+    L.cand1 = 0;
+    L.cand2 = arr;
+    L.count = (d == 5 ? 2 : 1) * arr;
+    L.list = L.count + 256;
+    L.total = L.list + (tasks * 4 + 255) / 256 * 256;
+    return L;
+}
+
+size_t dense_workspace_bytes(uint64_t n, uint32_t d) { return (size_t)dense_ws_layout(n, d).total; }
+
+uint32_t dense_decode_passes(const DecodeArgs& a, uint64_t l2_bytes) {
+    if (a.block || (a.d != 3 && a.d != 5) || (uint64_t)a.d * a.w * 4 <= l2_bytes / 3) return 1;
+    const uint32_t rpp = rows_per_pass(a.w, l2_bytes);
+    return (a.d + rpp - 1) / rpp;
+}
+
+cudaError_t launch_decode_dense_ws(const DecodeArgs& a, float* out, float* ws, cudaStream_t s) {
+    if (a.n == 0) return cudaSuccess;
+    DeviceInfo di{};
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return e;
+    if (dense_decode_passes(a, (uint64_t)di.l2_bytes) == 1) return launch_decode_dense(a, out, s);
+    const uint32_t rpp = rows_per_pass(a.w, (uint64_t)di.l2_bytes);
+    return a.d == 3 ? launch_dense_rows<3>(a, out, ws, rpp, s) : launch_dense_rows<5>(a, out, ws, rpp, s);
 }
 
 cudaError_t launch_tile_scan(const uint32_t* counts, uint64_t tiles, uint32_t* offsets, unsigned long long* total,

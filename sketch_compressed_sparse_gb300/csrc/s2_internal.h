@@ -93,6 +93,17 @@ struct DecodeArgs {
 };
 cudaError_t launch_decode_dense(const DecodeArgs& a, float* out, cudaStream_t s);
 
+// Dense decode that takes the median in passes over groups of rows when the
+// summed sketch is larger than a third of L2 (d = 3 or 5, element bitmap);
+// otherwise the same launches as launch_decode_dense. ws: dense_workspace_bytes.
+struct DenseWsLayout {
+    uint64_t cand1, cand2, count, list, total;  // byte offsets
+};
+DenseWsLayout dense_ws_layout(uint64_t n, uint32_t d);
+size_t dense_workspace_bytes(uint64_t n, uint32_t d);
+uint32_t dense_decode_passes(const DecodeArgs& a, uint64_t l2_bytes);
+cudaError_t launch_decode_dense_ws(const DecodeArgs& a, float* out, float* ws, cudaStream_t s);
+
 constexpr int kCompactTileWords = 256;  // 8192 positions per tile
 uint64_t compact_tiles(uint64_t nw);
 size_t compact_workspace_bytes(uint64_t n);

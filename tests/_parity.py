@@ -82,9 +82,12 @@ def gpu_pipeline(grad: torch.Tensor, d: int, w: int, seed: int, scale: float = 1
     bitmap = torch.empty(s2.nwords(n), dtype=torch.int32, device=dev)
     sketch = torch.empty((d, w), dtype=torch.float32, device=dev)
     out = torch.empty(n, dtype=torch.float32, device=dev)
+    out_ws = torch.full((n,), float("nan"), dtype=torch.float32, device=dev)
+    dws = torch.empty(max(s2.s2_decode_dense_workspace_size(n, d, w), 1), dtype=torch.uint8, device=dev)
     s2.s2_encode_batched(grad, d, w, seed, bitmaps, sketches, stream=stream)
     s2.s2_reduce(bitmaps, sketches, n, d, w, bitmap, sketch, stream=stream)
     s2.s2_decode_dense(bitmap, sketch, n, d, w, seed, out, scale=scale, stream=stream)
+    s2.s2_decode_dense_ws(bitmap, sketch, n, d, w, seed, out_ws, dws, scale=scale, stream=stream)
     res = {}
     if compact:
         ws = torch.empty(max(s2.s2_decode_workspace_size(n), 1), dtype=torch.uint8, device=dev)
@@ -97,7 +100,7 @@ def gpu_pipeline(grad: torch.Tensor, d: int, w: int, seed: int, scale: float = 1
         stream.synchronize()
     torch.cuda.synchronize()
     res.update(bitmaps=u32(bitmaps), sketches=sketches.cpu().numpy(), bitmap=u32(bitmap),
-               sketch=sketch.cpu().numpy(), out=out.cpu().numpy())
+               sketch=sketch.cpu().numpy(), out=out.cpu().numpy(), out_ws=out_ws.cpu().numpy())
     if compact:
         idx, val, cnt = res["compact"]
         c = int(cnt.item())
@@ -134,6 +137,9 @@ def check_pipeline(host_grad: np.ndarray, dtype: str, got: dict, d: int, w: int,
         assert_decoded_close(got["out"], ref["out"], ref["amax"], scale, cmax=cmax)
     unset = ~unpack(ref["bitmap"], n)
     assert (got["out"].view(np.uint32)[unset] == 0).all(), "unset positions must be exactly +0.0"
+    if "out_ws" in got:  # the dense decode with a workspace (row passes for large sketches) selects the same values
+        np.testing.assert_array_equal(got["out_ws"], got["out"])
+        assert (got["out_ws"].view(np.uint32)[unset] == 0).all(), "unset positions must be exactly +0.0"
     if "count" in got:
         cnt, idx, val, amax = oracle.decode_compact(ref["bitmap"], ref["S_sum"], n, seed, scale, ref["A_sum"])
         assert got["count"] == cnt

@@ -148,8 +148,24 @@ def test_hash_and_pipeline_errors(lib):
     pws = _fn(lib, "s2_pipeline_workspace_size", [I32, U32, U64, Params, ctypes.POINTER(SZ)])
     b = SZ()
     assert pws(0, 8, 1 << 20, Params(5, 1 << 10, 0), ctypes.byref(b)) == OK
-    # grad + bitmaps + sketches + bitmap + sketch + out, each rounded to 256 bytes
-    assert b.value == 8 * (1 << 22) + 8 * (1 << 17) + 8 * 5 * (1 << 12) + (1 << 17) + 5 * (1 << 12) + (1 << 22)
+    # grad + bitmaps + sketches + bitmap + sketch + out + the dense decode's
+    # workspace (for d = 5: two arrays of n floats, a 256-byte count and one
+    # 32-bit id per 512 positions), each rounded to 256 bytes
+    assert b.value == (8 * (1 << 22) + 8 * (1 << 17) + 8 * 5 * (1 << 12) + (1 << 17) + 5 * (1 << 12) + (1 << 22)
+                       + 2 * (1 << 22) + 256 + 4 * 2048)
+    dws = _fn(lib, "s2_decode_dense_workspace_size", [U64, Params, ctypes.POINTER(SZ)])
+    c = SZ()
+    assert dws(1000, Params(5, 64, 0), ctypes.byref(c)) == OK and c.value == 2 * 4 * 1024 + 256 + 256
+    assert dws(1000, Params(3, 64, 0), ctypes.byref(c)) == OK and c.value == 4 * 1024 + 256 + 256
+    assert dws(1000, Params(4, 64, 0), ctypes.byref(c)) == OK and c.value == 0
+    assert dws(1000, Params(0, 64, 0), ctypes.byref(c)) == INVALID
+    dd = _fn(lib, "s2_decode_dense_ws", [VP, VP, U64, Params, F32, VP, VP, SZ, VP])
+    ws_ok = 2 * 4 * 1024 + 512
+    assert dd(A, A + (1 << 20), 1000, Params(5, 64, 0), 1.0, A + (2 << 20), A + (3 << 20), ws_ok - 1, None) == INVALID
+    assert dd(A, A + (1 << 20), 1000, Params(5, 64, 0), 1.0, A + (2 << 20), A + (3 << 20) + 8, ws_ok, None) == ALIGN
+    assert dd(A, A + (1 << 20), 1000, Params(5, 64, 0), 1.0, A + (2 << 20), A + (2 << 20) + 16, ws_ok, None) == INVALID
+    assert dd(A, A + (1 << 20), 0, Params(5, 64, 0), 1.0, A + (2 << 20), None, 0, None) == OK
     p = _fn(lib, "s2_pipeline_dense_host", [VP, I32, U32, U64, Params, F32, VP, VP, SZ, VP])
     assert p(A, 0, 8, 1 << 20, Params(5, 1 << 10, 0), 1.0, A, A + 16, b.value - 1, None) == INVALID
     assert p(A, 0, 8, 1 << 20, Params(5, 1 << 10, 0), 1.0, A, A + 8, b.value, None) == ALIGN
+
