@@ -18,7 +18,8 @@
 // The select runs on many thread blocks per worker: each radix pass is one
 // launch that adds the digit counts of its slice of the norms into a global
 // 256-bin histogram per worker (every block first replays the earlier
-// passes' histograms to find the prefix it must match); a counting launch
+// passes' histograms, one thread per digit and a scan per pass, to find the
+// prefix it must match); a counting launch
 // and a marking launch then keep every norm above the final threshold and,
 // of the norms equal to it, the first ones in index order (each block starts
 // its rank after the equal norms of the blocks before it). No launch waits on
@@ -28,9 +29,12 @@
 namespace s2 {
 namespace {
 
-// Squared norm of block x of worker k, one warp per (k, x) task.
+// Squared norm of block x of worker k, one warp per (k, x) task. acc =
+// grad + residual is written back into the residual array (each element by
+// the thread that reads it): it is the new residual of every block that is
+// not kept, so the apply step only touches kept blocks' values.
 __global__ void __launch_bounds__(kThreads)
-    topk_norms_kernel(const float* __restrict__ grad, const float* __restrict__ resid, uint64_t n, uint32_t block,
+    topk_norms_kernel(const float* __restrict__ grad, float* __restrict__ resid, uint64_t n, uint32_t block,
                       uint64_t nb, uint32_t W, float* __restrict__ norms) {
     const int lane = threadIdx.x & 31;
     const uint64_t tasks = (uint64_t)W * nb;
@@ -42,7 +46,12 @@ __global__ void __launch_bounds__(kThreads)
         float s = 0.f;
 #pragma unroll 8
         for (uint64_t j = lane; j < len; j += 32) {
-            const float a = __fadd_rn(ld_stream_f32(grad + base + j), __ldg(resid + base + j));
+            // plain loads for both arrays: with the residual stored in the
+            // same kernel, evict-first (.cs) loads measured 2-12 times slower
+            // on this GPU (8 x 25.6 M floats: 0.54 ms with plain loads, 1.21
+            // ms with an evict-first gradient load, 3.57 ms with both)
+            const float a = __fadd_rn(grad[base + j], resid[base + j]);
+            resid[base + j] = a;
             s = __fmaf_rn(a, a, s);
         }
 #pragma unroll
@@ -58,27 +67,48 @@ static_assert(kSelThreads == 256, "one thread per histogram bin");
 
 // The radix state after `passes` passes of worker k: the digits fixed so far
 // (prefix under pmask) and how many norms equal to that prefix are still to
-// be kept. hist: [4][W][256] digit counts of the passes (pass-major).
+// be kept. hist: [4][W][256] digit counts of the passes (pass-major). Run by
+// all kSelThreads threads of the block, one per digit: per pass an inclusive
+// scan of the counts from digit 255 down finds the first digit at which the
+// count of norms at or above it reaches the number still to keep. The result
+// is left in *s_prefix, *s_pmask, *s_rest (shared); the call ends with a
+// __syncthreads.
 __device__ void select_state(const uint32_t* __restrict__ hist, uint32_t W, uint32_t k, int passes, uint64_t K,
-                             uint32_t* prefix, uint32_t* pmask, uint64_t* rest) {
-    uint32_t pf = 0, pm = 0;
-    uint64_t r = K;
-    for (int p = 0; p < passes; ++p) {
-        const uint32_t* h = hist + ((uint64_t)p * W + k) * 256;
-        const int shift = 24 - 8 * p;
-        uint64_t above = 0;
-        int dg = 255;
-        for (; dg > 0; --dg) {
-            if (above + h[dg] >= r) break;
-            above += h[dg];
-        }
-        pf |= (uint32_t)dg << shift;
-        pm |= 255u << shift;
-        r -= above;
+                             uint32_t* s_prefix, uint32_t* s_pmask, unsigned long long* s_rest) {
+    __shared__ uint32_t s_wsum[kSelThreads / 32];
+    __shared__ uint32_t s_first;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    if (t == 0) {
+        *s_prefix = 0u;
+        *s_pmask = 0u;
+        *s_rest = K;
     }
-    *prefix = pf;
-    *pmask = pm;
-    *rest = r;
+    __syncthreads();
+    for (int p = 0; p < passes; ++p) {
+        const uint32_t dg = 255u - (uint32_t)t;  // thread t holds digit 255 - t
+        const uint32_t c = hist[((uint64_t)p * W + k) * 256 + dg];
+        uint32_t incl = c;  // norms (matching the prefix) with digit in [dg, 255]
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) s_wsum[warp] = incl;
+        if (t == 0) s_first = kSelThreads - 1;  // no digit reaches it: digit 0
+        __syncthreads();
+        for (int w = 0; w < warp; ++w) incl += s_wsum[w];
+        const unsigned long long r = *s_rest;
+        const unsigned hit = __ballot_sync(kFull, incl >= r);
+        if (hit && lane == __ffs(hit) - 1) atomicMin(&s_first, (uint32_t)t);
+        __syncthreads();
+        if (t == (int)s_first) {  // above = the norms with a digit above dg
+            const int shift = 24 - 8 * p;
+            *s_prefix |= dg << shift;
+            *s_pmask |= 255u << shift;
+            *s_rest = r - (incl - c);
+        }
+        __syncthreads();
+    }
 }
 
 // Pass `pass` of the radix select: digit counts of the norms that match the
@@ -88,13 +118,10 @@ __global__ void __launch_bounds__(kSelThreads)
                      uint32_t* __restrict__ hist) {
     __shared__ uint32_t s_hist[256];
     __shared__ uint32_t s_prefix, s_pmask;
+    __shared__ unsigned long long s_rest;
     const uint32_t k = blockIdx.x;
-    if (threadIdx.x == 0) {
-        uint64_t rest;
-        select_state(hist, W, k, pass, K, &s_prefix, &s_pmask, &rest);
-    }
     s_hist[threadIdx.x] = 0;  // kSelThreads == 256 bins
-    __syncthreads();
+    select_state(hist, W, k, pass, K, &s_prefix, &s_pmask, &s_rest);  // ends with __syncthreads
     const uint32_t prefix = s_prefix, pmask = s_pmask;
     const int shift = 24 - 8 * pass;
     const uint32_t* key = reinterpret_cast<const uint32_t*>(norms) + (uint64_t)k * nb;
@@ -119,15 +146,11 @@ __global__ void __launch_bounds__(kSelThreads)
 __global__ void __launch_bounds__(kSelThreads)
     topk_eq_kernel(const float* __restrict__ norms, uint64_t nb, uint64_t K, uint32_t W,
                    const uint32_t* __restrict__ hist, uint32_t* __restrict__ eq_counts) {
-    __shared__ uint32_t s_thr;
+    __shared__ uint32_t s_thr, s_pm;
+    __shared__ unsigned long long s_rest;
     __shared__ uint32_t s_warp[kSelThreads / 32];
     const uint32_t k = blockIdx.x;
-    if (threadIdx.x == 0) {
-        uint32_t pm;
-        uint64_t rest;
-        select_state(hist, W, k, 4, K, &s_thr, &pm, &rest);
-    }
-    __syncthreads();
+    select_state(hist, W, k, 4, K, &s_thr, &s_pm, &s_rest);  // ends with __syncthreads
     const uint32_t thr = s_thr;
     const uint32_t* key = reinterpret_cast<const uint32_t*>(norms) + (uint64_t)k * nb;
     const uint64_t x0 = (uint64_t)blockIdx.y * kSelSlice;
@@ -154,7 +177,7 @@ __global__ void __launch_bounds__(kSelThreads)
     topk_keep_kernel(const float* __restrict__ norms, uint64_t nb, uint64_t K, uint32_t W,
                      const uint32_t* __restrict__ hist, const uint32_t* __restrict__ eq_counts,
                      uint8_t* __restrict__ keep) {
-    __shared__ uint32_t s_thr;
+    __shared__ uint32_t s_thr, s_pm;
     __shared__ unsigned long long s_rest, s_base;
     __shared__ uint32_t s_scan[kSelThreads / 32];
     __shared__ unsigned long long s_part[kSelThreads / 32];
@@ -175,12 +198,8 @@ __global__ void __launch_bounds__(kSelThreads)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
     if (lane == 0) s_part[warp] = part;
-    __syncthreads();
+    select_state(hist, W, k, 4, K, &s_thr, &s_pm, &s_rest);  // ends with __syncthreads
     if (threadIdx.x == 0) {
-        uint32_t pm;
-        uint64_t rest;
-        select_state(hist, W, k, 4, K, &s_thr, &pm, &rest);
-        s_rest = rest;
         unsigned long long base = 0;
         for (int w = 0; w < kSelThreads / 32; ++w) base += s_part[w];
         s_base = base;
@@ -209,12 +228,16 @@ __global__ void __launch_bounds__(kSelThreads)
 }
 
 // sparse = acc on kept blocks, 0 elsewhere; residual = acc elsewhere, 0 on
-// kept blocks. VEC: worker rows are 16-byte aligned (n % 4 == 0), so every
-// block (a multiple of 32 elements) starts on a 16-byte boundary.
+// kept blocks, where acc is already in the residual array (written by
+// topk_norms_kernel): a kept block moves its values from the residual to
+// sparse and zeroes them in the residual; any other block writes zeros to
+// sparse and leaves its residual as it is. VEC: worker rows are 16-byte
+// aligned (n % 4 == 0), so every block (a multiple of 32 elements) starts
+// on a 16-byte boundary.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads)
-    topk_apply_kernel(const float* __restrict__ grad, float* __restrict__ resid, const uint8_t* __restrict__ keep,
-                      uint64_t n, uint32_t block, uint64_t nb, uint32_t W, float* __restrict__ sparse) {
+    topk_apply_kernel(float* __restrict__ resid, const uint8_t* __restrict__ keep, uint64_t n, uint32_t block,
+                      uint64_t nb, uint32_t W, float* __restrict__ sparse) {
     const int lane = threadIdx.x & 31;
     const uint64_t tasks = (uint64_t)W * nb;
     const uint64_t nwarps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
@@ -222,26 +245,30 @@ __global__ void __launch_bounds__(kThreads)
         const uint64_t k = t / nb, x = t - k * nb;
         const uint64_t base = k * n + x * block;
         const uint64_t len = (x + 1) * block <= n ? block : n - x * block;
-        const bool kept = keep[t] != 0;
+        const bool kept = keep[t] != 0;  // warp-uniform
         uint64_t j0 = 0;
         if (VEC) {
             const uint64_t len4 = len / 4;
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
             for (uint64_t j = lane; j < len4; j += 32) {
-                const uint4 g = ld_stream_u4(grad + base + 4 * j);
-                const float4 r = reinterpret_cast<const float4*>(resid + base)[j];
-                const float4 a = make_float4(__fadd_rn(__uint_as_float(g.x), r.x), __fadd_rn(__uint_as_float(g.y), r.y),
-                                             __fadd_rn(__uint_as_float(g.z), r.z), __fadd_rn(__uint_as_float(g.w), r.w));
-                const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-                reinterpret_cast<float4*>(sparse + base)[j] = kept ? a : z;
-                reinterpret_cast<float4*>(resid + base)[j] = kept ? z : a;
+                if (kept) {
+                    float4* r4 = reinterpret_cast<float4*>(resid + base) + j;
+                    st_stream_f4(reinterpret_cast<float4*>(sparse + base) + j, *r4);
+                    st_stream_f4(r4, z);
+                } else {
+                    st_stream_f4(reinterpret_cast<float4*>(sparse + base) + j, z);
+                }
             }
             j0 = len4 * 4;
         }
         for (uint64_t j = j0 + lane; j < len; j += 32) {
-            const float a = __fadd_rn(ld_stream_f32(grad + base + j), resid[base + j]);
-            sparse[base + j] = kept ? a : 0.f;
-            resid[base + j] = kept ? 0.f : a;
+            if (kept) {
+                sparse[base + j] = resid[base + j];
+                resid[base + j] = 0.f;
+            } else {
+                sparse[base + j] = 0.f;
+            }
         }
     }
 }
@@ -302,11 +329,11 @@ cudaError_t launch_block_topk(const float* grad, float* resid, uint32_t W, uint6
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (n % 4 == 0)
-        topk_apply_kernel<true><<<grid_for(topk_apply_kernel<true>, blocks), kThreads, 0, s>>>(grad, resid, keep, n, block,
-                                                                                               nb, W, sparse);
+        topk_apply_kernel<true><<<grid_for(topk_apply_kernel<true>, blocks), kThreads, 0, s>>>(resid, keep, n, block, nb,
+                                                                                               W, sparse);
     else
-        topk_apply_kernel<false><<<grid_for(topk_apply_kernel<false>, blocks), kThreads, 0, s>>>(grad, resid, keep, n,
-                                                                                                 block, nb, W, sparse);
+        topk_apply_kernel<false><<<grid_for(topk_apply_kernel<false>, blocks), kThreads, 0, s>>>(resid, keep, n, block,
+                                                                                                 nb, W, sparse);
     return cudaGetLastError();
 }
 
