@@ -813,11 +813,22 @@ def run_e2e(args, wl, dev, s2):
         b.record(stream)
         b.synchronize()
         t += a.elapsed_time(b) / 1e3
-    return {"value": round(wl.W * wl.n * K / t / 1e9, 3), "unit": "Gelem/s",
-            "h2d_bytes_per_step": int(wl.W * wl.n * wl.elem_bytes), "d2h_bytes_per_step": int(4 * wl.n),
-            "steps": K, "ms_per_step": round(t / K * 1e3, 4),
-            "transfer": "pinned host gradient and output; the library's kernels read and write them in place "
-                        "(mapped page-locked memory), so the host<->device bytes move inside the kernels"}
+    h2d, d2h = int(wl.W * wl.n * wl.elem_bytes), int(4 * wl.n)
+    res = {"value": round(wl.W * wl.n * K / t / 1e9, 3), "unit": "Gelem/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "steps": K, "ms_per_step": round(t / K * 1e3, 4),
+           "transfer": "pinned host gradient and output; the library's kernels read and write them in place "
+                       "(mapped page-locked memory), so the host<->device bytes move inside the kernels"}
+    ceil = measured_ceilings()
+    link = (ceil or {}).get("host")
+    if link and link.get("sm_read_GBps") and link.get("sm_write_GBps"):
+        # the time the host link alone needs for this step's bytes, at the rates
+        # `bench.py --ceilings` measured for kernels reading and writing mapped host memory
+        bound_ms = (h2d / link["sm_read_GBps"] + d2h / link["sm_write_GBps"]) / 1e6
+        res["host_link"] = {"bound_ms_per_step": round(bound_ms, 4), "frac": round(bound_ms / (t / K * 1e3), 4),
+                            "read_GBps": link["sm_read_GBps"], "write_GBps": link["sm_write_GBps"],
+                            "source": "bench.py --ceilings (profiles/ceilings_gb300.json)"}
+    return res
 
 
 # ---------------------------------------------------------------- reference arm (the oracle)

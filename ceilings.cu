@@ -7,11 +7,18 @@
 //   read_and_red  both of the above in one kernel, interleaved  (do they share a ceiling?)
 //   red_v4_f32    random red.global.add.v4.f32 (4 adds per op)  (cost per op or per float?)
 //   smem_atomic   random shared-memory atomicAdd over 192 KiB   (on-chip alternative)
+//   concurrent    the stream and the reductions (and a zero write and the
+//                 gathers) as two kernels on two streams at once, half the
+//                 grid each                                      (do they overlap?)
+//   host_*        page-locked host memory mapped into the device: SM reads
+//                 and writes of 1 GiB in place, and copy-engine copies of
+//                 1 GiB each way                                 (the host link)
 //
 // Every index is masked to its buffer; no kernel waits on another.
 // Prints one JSON object on stdout.
 #include <cstdint>
 #include <cstdio>
+#include <cstring>
 #include <cuda_runtime.h>
 
 namespace {
@@ -66,6 +73,13 @@ __global__ void red_v4(float* sk, uint32_t mask4, uint64_t nops) {
         float* p = sk + 4 * (mix((uint32_t)x * 2654435761u) & mask4);
         asm volatile("red.global.add.v4.f32 [%0], {%1,%1,%1,%1};" ::"l"(p), "f"(1.0f) : "memory");
     }
+}
+
+// Zero 16-byte vectors with evict-first stores.
+__global__ void write_zero(uint4* dst, uint64_t n4) {
+    const uint64_t nth = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t x = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; x < n4; x += nth)
+        asm volatile("st.global.cs.v4.u32 [%0], {%1,%1,%1,%1};" ::"l"(dst + x), "r"(0u) : "memory");
 }
 
 constexpr uint32_t kSmemFloats = 48 * 1024;
@@ -132,6 +146,58 @@ int main() {
         smem_atomic<<<sms, 1024, kSmemFloats * 4>>>(per, fsink);
         ms[5] = t.stop();
     }
+    // the same work split over two streams at once, half the grid each
+    cudaStream_t s1, s2;
+    cudaStreamCreateWithFlags(&s1, cudaStreamNonBlocking);
+    cudaStreamCreateWithFlags(&s2, cudaStreamNonBlocking);
+    cudaEvent_t e1, e2;
+    cudaEventCreate(&e1);
+    cudaEventCreate(&e2);
+    uint4* dst = nullptr;
+    float cms[4] = {0};
+    if (cudaMalloc(&dst, src_bytes) == cudaSuccess) {
+        for (int rep = 0; rep < 2; ++rep) {
+            t.start();
+            cudaEventRecord(e1, 0);
+            cudaStreamWaitEvent(s1, e1, 0);
+            cudaStreamWaitEvent(s2, e1, 0);
+            read_red<<<grid / 2, block, 0, s1>>>(src, n4, sk, mask, nred, 1, 0, usink);
+            read_red<<<grid / 2, block, 0, s2>>>(src, n4, sk, mask, nred, 0, 1, usink);
+            cudaEventRecord(e1, s1);
+            cudaEventRecord(e2, s2);
+            cudaStreamWaitEvent(0, e1, 0);
+            cudaStreamWaitEvent(0, e2, 0);
+            cms[0] = t.stop();
+            t.start(); write_zero<<<grid, block>>>(dst, n4); cms[1] = t.stop();
+            t.start();
+            cudaEventRecord(e1, 0);
+            cudaStreamWaitEvent(s1, e1, 0);
+            cudaStreamWaitEvent(s2, e1, 0);
+            write_zero<<<grid / 2, block, 0, s1>>>(dst, n4);
+            gather<<<grid / 2, block, 0, s2>>>(sk, mask, nred, fsink);
+            cudaEventRecord(e1, s1);
+            cudaEventRecord(e2, s2);
+            cudaStreamWaitEvent(0, e1, 0);
+            cudaStreamWaitEvent(0, e2, 0);
+            cms[2] = t.stop();
+        }
+        cudaFree(dst);
+    }
+    // the host link: mapped page-locked memory read and written by kernels in place, and copies
+    void* host = nullptr;
+    void* hdev = nullptr;
+    float hms[4] = {0};
+    if (cudaHostAlloc(&host, src_bytes, cudaHostAllocMapped) == cudaSuccess &&
+        cudaHostGetDevicePointer(&hdev, host, 0) == cudaSuccess) {
+        memset(host, 0, src_bytes);
+        for (int rep = 0; rep < 2; ++rep) {
+            t.start(); read_red<<<grid, block>>>(static_cast<const uint4*>(hdev), n4, sk, mask, nred, 1, 0, usink); hms[0] = t.stop();
+            t.start(); write_zero<<<grid, block>>>(static_cast<uint4*>(hdev), n4); hms[1] = t.stop();
+            t.start(); cudaMemcpyAsync(src, host, src_bytes, cudaMemcpyHostToDevice, 0); hms[2] = t.stop();
+            t.start(); cudaMemcpyAsync(host, src, src_bytes, cudaMemcpyDeviceToHost, 0); hms[3] = t.stop();
+        }
+        cudaFreeHost(host);
+    }
     const cudaError_t e = cudaDeviceSynchronize();
     const double sector = 32.0;
     printf("{\"sms\": %d, \"l2_bytes\": %d, "
@@ -140,9 +206,16 @@ int main() {
            "\"gather_f32\": {\"ms\": %.4f, \"Gops_per_s\": %.1f}, "
            "\"read_and_red\": {\"ms\": %.4f, \"sum_of_alone_ms\": %.4f}, "
            "\"red_v4_f32\": {\"ms\": %.4f, \"Gops_per_s\": %.1f, \"Gadds_per_s\": %.1f}, "
-           "\"smem_atomic\": {\"ms\": %.4f, \"Gops_per_s\": %.1f}, \"status\": \"%s\"}\n",
+           "\"smem_atomic\": {\"ms\": %.4f, \"Gops_per_s\": %.1f}, "
+           "\"concurrent\": {\"read_and_red_two_streams_ms\": %.4f, \"write_ms\": %.4f, "
+           "\"write_and_gather_two_streams_ms\": %.4f, \"sum_of_alone_ms\": %.4f}, "
+           "\"host\": {\"sm_read_GBps\": %.1f, \"sm_write_GBps\": %.1f, \"copy_h2d_GBps\": %.1f, "
+           "\"copy_d2h_GBps\": %.1f}, \"status\": \"%s\"}\n",
            sms, l2, ms[0], src_bytes / (ms[0] * 1e6), src_bytes / sector / (ms[0] * 1e6), ms[1], nred / (ms[1] * 1e6),
            ms[2], nred / (ms[2] * 1e6), ms[3], ms[0] + ms[1], ms[4], nred / 4 / (ms[4] * 1e6), nred / (ms[4] * 1e6),
-           ms[5], (double)sms * 1024 * per / (ms[5] * 1e6), cudaGetErrorString(e));
+           ms[5], (double)sms * 1024 * per / (ms[5] * 1e6), cms[0], cms[1], cms[2], cms[1] + ms[2],
+           hms[0] > 0 ? src_bytes / (hms[0] * 1e6) : 0.0, hms[1] > 0 ? src_bytes / (hms[1] * 1e6) : 0.0,
+           hms[2] > 0 ? src_bytes / (hms[2] * 1e6) : 0.0, hms[3] > 0 ? src_bytes / (hms[3] * 1e6) : 0.0,
+           cudaGetErrorString(e));
     return e == cudaSuccess ? 0 : 2;
 }
