@@ -139,12 +139,12 @@ def encode_launches(wl: workloads.Workload, l2_bytes: int, sms: int = 152) -> in
 
 
 def dense_decode_launches(n: int, l2_bytes: int, d: int = 0, w: int = 0, block: int = 0) -> int:
-    """Launches of one s2_decode_dense_ws call: a summed sketch larger than a
-    third of L2 (d = 3 or 5, element bitmap) is decoded by a zero launch and
-    one launch per group of rows that fits in a third of L2; otherwise a dense
-    output larger than L2 is written in two launches (zeros first), a smaller
-    one in one."""
-    budget = l2_bytes // 3
+    """Launches of one s2_decode_dense_ws call: a summed sketch larger than 2/5
+    of L2 (d = 3 or 5, element bitmap) is decoded by a zero launch and one
+    launch per group of rows that fits in 2/5 of L2; otherwise a dense output
+    larger than L2 is written in two launches (zeros first), a smaller one in
+    one."""
+    budget = l2_bytes * 2 // 5
     if not block and d in (3, 5) and 4 * d * w > budget:
         rpp = 1 if 4 * w >= budget else budget // (4 * w)
         return 1 + -(-d // rpp)

@@ -94,7 +94,7 @@ struct DecodeArgs {
 cudaError_t launch_decode_dense(const DecodeArgs& a, float* out, cudaStream_t s);
 
 // Dense decode that takes the median in passes over groups of rows when the
-// summed sketch is larger than a third of L2 (d = 3 or 5, element bitmap);
+// summed sketch is larger than 2/5 of L2 (d = 3 or 5, element bitmap);
 // otherwise the same launches as launch_decode_dense. ws: dense_workspace_bytes.
 struct DenseWsLayout {
     uint64_t cand1, cand2, count, list, total;  // byte offsets

@@ -1,14 +1,15 @@
 """GPU parity of the dense decode taken in passes over groups of rows
-(s2_decode_dense_ws), for summed sketches larger than a third of L2.
+(s2_decode_dense_ws), for summed sketches larger than 2/5 of L2.
 
 The median query of Algorithm 1 ("S2 Reducer", Section 3.1 "Decompressing
 Sparse Gradient") only selects among the d row values of a position (odd d),
 so on a planted float32 sketch the result must match the oracle bit for bit
 whatever the order in which the rows are visited. The cases cover every pass
-plan on a GB300 (L2 of 135.5 MB, a third of it per pass): 2 rows per pass
-(d = 5, w = 2^22: 16.8 MB rows), 1 row per pass (w = 2^23; after the third
-row three candidates are carried), 3 rows per pass (w = 3 * 2^20 + 7), and
-d = 3 with 2 + 1 rows; ragged lengths and a scale other than one.
+plan on a GB300 (L2 of 135.5 MB, 2/5 of it per pass): for d = 5, 3 rows per
+pass (w = 2^22: 16.8 MB rows; three candidates carried after the first
+pass), 1 row per pass (w = 2^23), 4 rows per pass (w = 3 * 2^20 + 7) and 2
+rows per pass (w = 5,000,003); for d = 3, 2 + 1 rows (w = 5,000,001) and one
+row per pass (w = 2^23); ragged lengths and a scale other than one.
 """
 import numpy as np
 import pytest
@@ -41,7 +42,8 @@ def _decode_ws(B, S, n, d, w, seed, scale):
     (5, 1 << 22, 3_000_017, 0.2, 1.0),
     (5, 1 << 23, 1_000_003, 0.3, 0.5),
     (5, 3 * (1 << 20) + 7, 2_000_000, 0.05, 1.0),
-    (3, (1 << 22) + 3, 1_048_579, 0.5, 2.0),
+    (5, 5_000_003, 1_500_001, 0.1, 1.0),
+    (3, 5_000_001, 1_048_579, 0.5, 2.0),
     (3, 1 << 23, 777_777, 1.0, 1.0),  # every position set
 ])
 def test_row_pass_decode_is_bit_exact(d, w, n, density, scale):
