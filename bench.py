@@ -147,7 +147,8 @@ def dense_decode_launches(n: int, l2_bytes: int, d: int = 0, w: int = 0, block: 
     budget = l2_bytes * 2 // 5
     if not block and d in (3, 5) and 4 * d * w > budget:
         rpp = 1 if 4 * w >= budget else budget // (4 * w)
-        return 1 + -(-d // rpp)
+        one_launch = 1 if 4 * d * w <= 96 << 20 else 0  # queued too, works when most tasks are set
+        return 1 + one_launch + -(-d // rpp)
     return 2 if 4 * n > l2_bytes else 1
 
 
@@ -767,7 +768,9 @@ def run_sweep(args):
     sub.warmup = max(3, args.warmup)
     t0 = time.perf_counter()
     for p in workloads.sweep_grid():
-        if p["n"] > (1 << args.sweep_max_log2):
+        if p["n"] > (1 << args.sweep_max_log2) or p["n"] < (1 << args.sweep_min_log2):
+            continue
+        if args.sweep_density is not None and p["density"] != args.sweep_density:
             continue
         wl = workloads.sweep_point(**p)
         r = run_ours(sub, wl, 1, 0, 0)
@@ -781,8 +784,10 @@ def run_sweep(args):
     peaks = measured_peaks()
     return {"metric": METRIC + " (sweep grid)", "unit": "Gelem/s", "n_gpus": 1, "steps_per_point": sub.steps,
             "warmup": sub.warmup, "higher_is_better": True, "data": "synthetic",
-            "config": {"workload": "sweep: W=8, n=2^20..2^%d, fp32/bf16, density 0.1/1/10 %%, d in {3,5}, "
-                                   "w = 2^round(log2(nnz/2))" % args.sweep_max_log2,
+            "config": {"workload": "sweep: W=8, n=2^%d..2^%d, fp32/bf16, density %s, d in {3,5}, "
+                                   "w = 2^round(log2(nnz/2))" % (args.sweep_min_log2, args.sweep_max_log2,
+                                                                 "0.1/1/10 %" if args.sweep_density is None
+                                                                 else f"{100 * args.sweep_density:g} %"),
                        "l2": "flushed before every step (512 MiB write)"},
             "hbm_peak_gbs": peaks["hbm_gbs"], "points": rows,
             "wall_s": round(time.perf_counter() - t0, 1)}
@@ -900,6 +905,10 @@ def main(argv=None):
                     help="large_lm per-worker run only: skip the embedding and top-k measurements in per_config")
     ap.add_argument("--sweep-max-log2", type=int, default=28,
                     help="--config sweep: largest gradient length as a power of two (20..28)")
+    ap.add_argument("--sweep-min-log2", type=int, default=20,
+                    help="--config sweep: smallest gradient length as a power of two (20..28)")
+    ap.add_argument("--sweep-density", type=float, default=None, choices=[0.001, 0.01, 0.1],
+                    help="--config sweep: only the points of this density")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle timing")
     ap.add_argument("--e2e-steps", type=int, default=20)

@@ -267,7 +267,10 @@ S2_API s2_status s2_decode_dense_blocks(const uint32_t *block_bitmap, const floa
  * 512-position stretch without a set bit and lists the others; each pass then
  * reads only its rows for every set position of the listed stretches and
  * carries the candidates for the median that remain (at most 2 for d = 3, 3
- * for d = 5) to the next pass in `out` and the workspace. The
+ * for d = 5) to the next pass in `out` and the workspace. A sketch of at most
+ * 96 MB whose set positions reach at least half of the stretches is decoded
+ * in one launch over all rows instead (the device picks, from the count of
+ * listed stretches). The
  * decoded values are the same as s2_decode_dense's (the median selects one
  * of the row values, or averages none); an estimate of zero may come out as
  * +0.0 or -0.0 as with s2_decode_dense. Otherwise the call launches exactly

@@ -108,8 +108,13 @@ __device__ __forceinline__ uint32_t lane_mask_blocks(const DecodeArgs& a, uint64
 // that the zero stream does not evict the summed sketch while the gathers
 // need it. Without PHASED every task is handled (and the kernel carries no
 // phase test).
+// guard (optional): the launch works only if *guard >= guard_at (a count
+// written by an earlier launch; the same for every thread).
 template <int D, bool BLK, bool PHASED>
-__global__ void __launch_bounds__(kThreads) decode_dense_kernel(DecodeArgs a, float* __restrict__ out, int set_tasks) {
+__global__ void __launch_bounds__(kThreads)
+    decode_dense_kernel(DecodeArgs a, float* __restrict__ out, int set_tasks,
+                        const unsigned int* __restrict__ guard = nullptr, uint32_t guard_at = 0) {
+    if (guard && *guard < guard_at) return;
     __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
     load_keys(a.keys, s_kh, s_ks);
     const int lane = threadIdx.x & 31;
@@ -250,41 +255,55 @@ __device__ __forceinline__ uint32_t task_word(const DecodeArgs& a, uint64_t wi, 
 
 // The launch before the passes: writes the 512 zeros of every task without a
 // set position and lists the others (task ids in any order, their number in
-// *count, which starts at zero) for the passes to work through.
+// *count, which starts at zero) for the passes to work through. A warp keeps
+// up to 32 ids in its lanes and appends them with one atomic.
 __global__ void __launch_bounds__(kThreads)
     decode_zero_list_kernel(DecodeArgs a, float* __restrict__ out, uint32_t* __restrict__ list,
                             unsigned int* __restrict__ count) {
     const int lane = threadIdx.x & 31;
     const uint64_t ntasks = (a.n + kTaskElems - 1) / kTaskElems;
     const uint64_t nwarps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
+    uint32_t held = 0;  // task ids held by the lanes (lane q holds the q-th), warp-uniform
+    uint32_t mine = 0;
+    auto flush = [&]() {
+        unsigned int base = 0;
+        if (lane == 0) base = atomicAdd(count, held);
+        base = __shfl_sync(kFull, base, 0);
+        if ((uint32_t)lane < held) list[base + lane] = mine;
+        held = 0;
+    };
     for (uint64_t t = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < ntasks; t += nwarps) {
         const uint32_t mask = lane_mask(task_word(a, t * kTaskWords + lane, lane), lane);
         if (__any_sync(kFull, mask != 0)) {
-            if (lane == 0) list[atomicAdd(count, 1u)] = (uint32_t)t;
+            if ((uint32_t)lane == held) mine = (uint32_t)t;
+            if (++held == 32) flush();
             continue;
         }
         const uint64_t e0 = t * kTaskElems;
 #pragma unroll
         for (int u = 0; u < 4; ++u) st_stream_f4_tail(out, e0 + u * 128 + lane * 4, a.n, make_float4(0.f, 0.f, 0.f, 0.f));
     }
+    if (held) flush();
 }
 
 // One pass over rows [j0, j1) of the median (D = 3 or 5), one warp per listed
 // task of 512 positions; a lane owns 4 chunks of 4 consecutive positions,
-// like decode_dense_kernel.
+// like decode_dense_kernel. The launch works only if fewer than dense_at
+// tasks are listed (otherwise the one-launch decode has done the work).
 template <int D>
 __global__ void __launch_bounds__(kThreads)
     decode_rows_kernel(DecodeArgs a, float* __restrict__ out, float* __restrict__ cand1,
                        float* __restrict__ cand2, const uint32_t* __restrict__ list,
-                       const unsigned int* __restrict__ count, int j0, int j1) {
+                       const unsigned int* __restrict__ count, int j0, int j1, uint32_t dense_at) {
     static_assert(D == 3 || D == 5, "row passes are specialised for 3 and 5 rows");
+    const uint32_t listed = *count;
+    if (listed >= dense_at) return;  // the same for every thread of the launch
     __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
     load_keys(a.keys, s_kh, s_ks);
     const int lane = threadIdx.x & 31;
     const uint64_t keep = policy_evict_last();
     const int k_in = kept_after(D, j0), k_out = kept_after(D, j1);
     const bool last = j1 == D;
-    const uint32_t listed = *count;
     const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
     for (uint32_t x = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; x < listed; x += nwarps) {
         const uint64_t t = list[x];
@@ -525,6 +544,10 @@ cudaError_t launch_dense_d(const DecodeArgs& a, float* out, cudaStream_t s) {
 // 0.395 ms, 4 rows 0.398 ms.
 uint64_t pass_budget(uint64_t l2_bytes) { return l2_bytes * 2 / 5; }
 
+// Largest summed sketch for which a decode with most tasks set runs in one
+// launch over all rows instead of in passes (see launch_dense_rows).
+constexpr uint64_t kOneLaunchMax = 96ull << 20;
+
 uint32_t rows_per_pass(uint64_t w, uint64_t l2_bytes) {
     const uint64_t budget = pass_budget(l2_bytes), row = 4 * w;
     return row >= budget ? 1u : (uint32_t)(budget / row);
@@ -545,10 +568,27 @@ cudaError_t launch_dense_rows(const DecodeArgs& a, float* out, float* ws, uint32
     decode_zero_list_kernel<<<grid_for(decode_zero_list_kernel, blocks), kThreads, 0, s>>>(a, out, list, count);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    // A sketch up to kOneLaunchMax whose set positions reach at least half of
+    // the tasks is decoded faster in one launch over all rows (the set-task
+    // launch of the two-launch decode) than in passes, which would then carry
+    // candidates for nearly every position (measured on 8 workers of 2^26
+    // positions at 10 % density, d = 5, an 84 MB sketch: 0.76 ms in one
+    // launch, 1.12 ms in passes; with 3 % of the tasks set, as in the large-LM
+    // workload with the same sketch, the passes win, 0.38 against 0.50 ms).
+    // Both forms are queued; the count of listed tasks picks one on the device.
+    uint32_t dense_at = 0xffffffffu;
+    if ((uint64_t)a.d * a.w * 4 <= kOneLaunchMax) {
+        dense_at = (uint32_t)((tasks + 1) / 2);
+        decode_dense_kernel<D, false, true>
+            <<<grid_for(decode_dense_kernel<D, false, true>, blocks), kThreads, 0, s>>>(a, out, 1, count, dense_at);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     const int grid = grid_for(decode_rows_kernel<D>, blocks);
     for (uint32_t j0 = 0; j0 < (uint32_t)D; j0 += rpp) {
         const uint32_t j1 = j0 + rpp < (uint32_t)D ? j0 + rpp : (uint32_t)D;
-        decode_rows_kernel<D><<<grid, kThreads, 0, s>>>(a, out, cand1, cand2, list, count, (int)j0, (int)j1);
+        decode_rows_kernel<D><<<grid, kThreads, 0, s>>>(a, out, cand1, cand2, list, count, (int)j0, (int)j1,
+                                                         dense_at);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -70,10 +70,11 @@ def test_dense_decode_launches():
     L2 = 135_528_448
     assert bench.dense_decode_launches(33_278 * 512, L2) == 1
     assert bench.dense_decode_launches(267_735 * 1024, L2) == 2  # 1.1 GB of output: zeros first
-    # an 84 MB summed sketch of 5 rows: a zero launch and passes over rows {0,1,2}, {3,4}
-    assert bench.dense_decode_launches(267_735 * 1024, L2, 5, 1 << 22) == 3
-    assert bench.dense_decode_launches(1 << 27, L2, 5, 1 << 23) == 6  # one 33.5 MB row per pass
-    assert bench.dense_decode_launches(1 << 27, L2, 3, 5_000_001) == 3  # 60 MB: {0,1}, {2}
+    # an 84 MB summed sketch of 5 rows: a zero launch, the one-launch form (which
+    # works only if most tasks are set) and passes over rows {0,1,2}, {3,4}
+    assert bench.dense_decode_launches(267_735 * 1024, L2, 5, 1 << 22) == 4
+    assert bench.dense_decode_launches(1 << 27, L2, 5, 1 << 23) == 6  # 168 MB: one 33.5 MB row per pass
+    assert bench.dense_decode_launches(1 << 27, L2, 3, 5_000_001) == 4  # 60 MB: one launch or {0,1}, {2}
     assert bench.dense_decode_launches(1 << 27, L2, 3, 1 << 22) == 2  # 50 MB: below 2/5 of L2
     assert bench.dense_decode_launches(1 << 27, L2, 4, 1 << 23) == 2  # even d: no row passes
     assert bench.dense_decode_launches(33_278 * 512, L2, 5, 1 << 20) == 1  # 21 MB sketch: one launch
