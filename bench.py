@@ -172,8 +172,9 @@ def kernel_source_sha() -> str:
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per encode launch from a committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
+    """DRAM bytes of one step's encode stage (its zero-fill and encode launches)
+    from a committed ncu summary, if it was taken on the current kernel sources
+    (else None)."""
     p = os.path.join(ROOT, "profiles", "encode_traffic.json")
     if not os.path.exists(p):
         return None
