@@ -4,8 +4,8 @@
 // carried into the next step's gradient).
 //
 // Per worker: acc = grad + residual; the squared norm of every block of
-// `block` elements in float32, one warp per block (lane l accumulates
-// fmaf(a, a, s) over elements l, l+32, ... of the block, then an XOR
+// `block` elements in float32, one warp per block (each lane accumulates
+// fmaf(a, a, s) over its block/32 elements in a fixed order, then an XOR
 // butterfly): a fixed order, so that which blocks are kept -- an integer
 // decision -- is the same on every run; the K-th largest norm by a 4-pass
 // 8-bit radix select over the norms' bit patterns (non-negative floats order
@@ -32,7 +32,17 @@ namespace {
 // Squared norm of block x of worker k, one warp per (k, x) task. acc =
 // grad + residual is written back into the residual array (each element by
 // the thread that reads it): it is the new residual of every block that is
-// not kept, so the apply step only touches kept blocks' values.
+// not kept, so the apply step only touches kept blocks' values. Plain loads
+// for both arrays: with the residual stored in the same kernel, evict-first
+// (.cs) loads measured 2-12 times slower on this GPU (8 x 25.6 M floats:
+// 0.54 ms with plain loads, 1.21 ms with an evict-first gradient load, 3.57
+// ms with both).
+// VEC (worker rows 16-byte aligned, block a multiple of 128): lane l takes
+// the 16-byte vectors at elements 4l + 128i, i = 0, 1, ..., adding their four
+// squares in order into one sum, so each lane still sums block/32 squares
+// (the rounding bound above holds as it is); otherwise lane l takes elements
+// l, l + 32, ... one at a time.
+template <bool VEC>
 __global__ void __launch_bounds__(kThreads)
     topk_norms_kernel(const float* __restrict__ grad, float* __restrict__ resid, uint64_t n, uint32_t block,
                       uint64_t nb, uint32_t W, float* __restrict__ norms) {
@@ -44,15 +54,27 @@ __global__ void __launch_bounds__(kThreads)
         const uint64_t base = k * n + x * block;
         const uint64_t len = (x + 1) * block <= n ? block : n - x * block;
         float s = 0.f;
+        if (VEC) {  // len is a multiple of 4 (n % 4 == 0, block % 128 == 0)
+            const float4* g4 = reinterpret_cast<const float4*>(grad + base);
+            float4* r4 = reinterpret_cast<float4*>(resid + base);
+#pragma unroll 4
+            for (uint64_t j = lane; j < len / 4; j += 32) {
+                const float4 g = g4[j], r = r4[j];
+                const float4 a = make_float4(__fadd_rn(g.x, r.x), __fadd_rn(g.y, r.y), __fadd_rn(g.z, r.z),
+                                             __fadd_rn(g.w, r.w));
+                r4[j] = a;
+                s = __fmaf_rn(a.x, a.x, s);
+                s = __fmaf_rn(a.y, a.y, s);
+                s = __fmaf_rn(a.z, a.z, s);
+                s = __fmaf_rn(a.w, a.w, s);
+            }
+        } else {
 #pragma unroll 8
-        for (uint64_t j = lane; j < len; j += 32) {
-            // plain loads for both arrays: with the residual stored in the
-            // same kernel, evict-first (.cs) loads measured 2-12 times slower
-            // on this GPU (8 x 25.6 M floats: 0.54 ms with plain loads, 1.21
-            // ms with an evict-first gradient load, 3.57 ms with both)
-            const float a = __fadd_rn(grad[base + j], resid[base + j]);
-            resid[base + j] = a;
-            s = __fmaf_rn(a, a, s);
+            for (uint64_t j = lane; j < len; j += 32) {
+                const float a = __fadd_rn(grad[base + j], resid[base + j]);
+                resid[base + j] = a;
+                s = __fmaf_rn(a, a, s);
+            }
         }
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) s = __fadd_rn(s, __shfl_xor_sync(kFull, s, off));
@@ -309,7 +331,12 @@ cudaError_t launch_block_topk(const float* grad, float* resid, uint32_t W, uint6
     uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
     uint32_t* eq = reinterpret_cast<uint32_t*>(ws + L.eq);
     const uint64_t blocks = ((uint64_t)W * nb + (kThreads / 32) - 1) / (kThreads / 32);
-    topk_norms_kernel<<<grid_for(topk_norms_kernel, blocks), kThreads, 0, s>>>(grad, resid, n, block, nb, W, norms);
+    if (n % 4 == 0 && block % 128 == 0)
+        topk_norms_kernel<true><<<grid_for(topk_norms_kernel<true>, blocks), kThreads, 0, s>>>(grad, resid, n, block,
+                                                                                               nb, W, norms);
+    else
+        topk_norms_kernel<false><<<grid_for(topk_norms_kernel<false>, blocks), kThreads, 0, s>>>(grad, resid, n, block,
+                                                                                                 nb, W, norms);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const dim3 grid(W, (unsigned)L.slices);  // slices <= 65535: nb < 2^28 for n < 2^32

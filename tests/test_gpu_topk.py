@@ -98,6 +98,7 @@ def check_worker(G, E, block, K, sp, E_new):
     (2, 5_000, 1024, 2),
     (2, 32 * 20_000, 32, 625),   # 20,000 blocks: the select spans 5 thread blocks per worker
     (1, 32 * 70_001 + 7, 32, 2187),  # 17 slices, ragged last block
+    (2, 128 * 9_000 + 132, 128, 400),  # 16-byte vector norms; ragged last block of 132
 ])
 def test_block_topk_keeps_a_valid_largest_set(W, n, block, K):
     G = laplace_grads(W, n, tag=W * 7 + K)
@@ -134,12 +135,13 @@ def test_block_topk_ties_across_thread_blocks_of_the_select():
         check_worker(G[k], np.zeros_like(G[k]), block, K, sp[k], e[k])
 
 
-def test_block_topk_repeated_patterns_match_the_oracle_exactly():
+@pytest.mark.parametrize("block", [64, 256])  # 4-byte and 16-byte loads in the norms
+def test_block_topk_repeated_patterns_match_the_oracle_exactly(block):
     # Every block is one of four fixed patterns with well separated norms, so
     # equal norms are exactly equal on both sides and the kept set is unique:
     # K falls inside the group of the second largest pattern, whose members
     # are spread over all of the select's slices.
-    nb, block = 24_000, 64
+    nb = 24_000
     rng = np.random.default_rng(77)
     pats = rng.normal(size=(4, block)).astype(np.float32) * np.array([[1.0], [2.0], [3.0], [4.0]], np.float32)
     choice = rng.integers(0, 4, size=nb)
