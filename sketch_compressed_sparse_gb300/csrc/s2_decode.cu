@@ -272,16 +272,31 @@ __global__ void __launch_bounds__(kThreads)
         if ((uint32_t)lane < held) list[base + lane] = mine;
         held = 0;
     };
-    for (uint64_t t = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < ntasks; t += nwarps) {
-        const uint32_t mask = lane_mask(task_word(a, t * kTaskWords + lane, lane), lane);
-        if (__any_sync(kFull, mask != 0)) {
-            if ((uint32_t)lane == held) mine = (uint32_t)t;
-            if (++held == 32) flush();
-            continue;
-        }
-        const uint64_t e0 = t * kTaskElems;
+    // the bitmap words of a warp's next kAhead tasks are loaded together, so
+    // the zero stores of one task do not wait for the next task's word
+    constexpr int kAhead = 4;
+    for (uint64_t t0 = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t0 < ntasks; t0 += kAhead * nwarps) {
+        uint32_t words[kAhead];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) st_stream_f4_tail(out, e0 + u * 128 + lane * 4, a.n, make_float4(0.f, 0.f, 0.f, 0.f));
+        for (int q = 0; q < kAhead; ++q) {
+            const uint64_t t = t0 + q * nwarps;
+            words[q] = t < ntasks ? task_word(a, t * kTaskWords + lane, lane) : 0u;
+        }
+#pragma unroll
+        for (int q = 0; q < kAhead; ++q) {
+            const uint64_t t = t0 + q * nwarps;
+            if (t >= ntasks) break;  // warp-uniform
+            const uint32_t mask = lane_mask(words[q], lane);
+            if (__any_sync(kFull, mask != 0)) {
+                if ((uint32_t)lane == held) mine = (uint32_t)t;
+                if (++held == 32) flush();
+                continue;
+            }
+            const uint64_t e0 = t * kTaskElems;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                st_stream_f4_tail(out, e0 + u * 128 + lane * 4, a.n, make_float4(0.f, 0.f, 0.f, 0.f));
+        }
     }
     if (held) flush();
 }
@@ -585,12 +600,17 @@ cudaError_t launch_dense_rows(const DecodeArgs& a, float* out, float* ws, uint32
         if (e != cudaSuccess) return e;
     }
     const int grid = grid_for(decode_rows_kernel<D>, blocks);
-    for (uint32_t j0 = 0; j0 < (uint32_t)D; j0 += rpp) {
-        const uint32_t j1 = j0 + rpp < (uint32_t)D ? j0 + rpp : (uint32_t)D;
+    // The smallest group of rows goes first: fewer candidates are carried
+    // after it (d = 5 in groups of 3: rows {0, 1} then {2, 3, 4}, two
+    // candidates instead of three).
+    const uint32_t passes = ((uint32_t)D + rpp - 1) / rpp;
+    for (uint32_t p = 0, j0 = 0; p < passes; ++p) {
+        const uint32_t j1 = j0 + (p == 0 ? (uint32_t)D - rpp * (passes - 1) : rpp);
         decode_rows_kernel<D><<<grid, kThreads, 0, s>>>(a, out, cand1, cand2, list, count, (int)j0, (int)j1,
                                                          dense_at);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
+        j0 = j1;
     }
     return cudaSuccess;
 }

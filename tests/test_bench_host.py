@@ -71,7 +71,7 @@ def test_dense_decode_launches():
     assert bench.dense_decode_launches(33_278 * 512, L2) == 1
     assert bench.dense_decode_launches(267_735 * 1024, L2) == 2  # 1.1 GB of output: zeros first
     # an 84 MB summed sketch of 5 rows: a zero launch, the one-launch form (which
-    # works only if most tasks are set) and passes over rows {0,1,2}, {3,4}
+    # works only if most tasks are set) and passes over rows {0,1}, {2,3,4}
     assert bench.dense_decode_launches(267_735 * 1024, L2, 5, 1 << 22) == 4
     assert bench.dense_decode_launches(1 << 27, L2, 5, 1 << 23) == 6  # 168 MB: one 33.5 MB row per pass
     assert bench.dense_decode_launches(1 << 27, L2, 3, 5_000_001) == 4  # 60 MB: one launch or {0,1}, {2}

@@ -5,13 +5,14 @@ The median query of Algorithm 1 ("S2 Reducer", Section 3.1 "Decompressing
 Sparse Gradient") only selects among the d row values of a position (odd d),
 so on a planted float32 sketch the result must match the oracle bit for bit
 whatever the order in which the rows are visited. The cases cover every plan
-on a GB300 (L2 of 135.5 MB, 2/5 of it per pass): for d = 5, 3 rows per pass
-(w = 2^22: 16.8 MB rows; three candidates carried after the first pass), 1
-row per pass (w = 2^23), 4 rows per pass (w = 3 * 2^20 + 7) and 2 rows per
-pass (w = 5,000,003); for d = 3, 2 + 1 rows (w = 5,000,001) and one row per
-pass (w = 2^23); and the one-launch form over all rows, which a sketch of at
-most 96 MB takes when at least half of the 512-position tasks hold a set
-position; ragged lengths and a scale other than one.
+on a GB300 (L2 of 135.5 MB, 2/5 of it per pass; the smallest group of rows
+first): for d = 5, groups of 3 rows (w = 2^22: 16.8 MB rows; rows {0, 1},
+then {2, 3, 4} from two carried candidates), 1 row per pass (w = 2^23), 4
+rows per pass (w = 3 * 2^20 + 7) and 2 rows per pass (w = 5,000,003); for
+d = 3, 1 + 2 rows (w = 5,000,001) and one row per pass (w = 2^23); and the
+one-launch form over all rows, which a sketch of at most 96 MB takes when at
+least half of the 512-position tasks hold a set position; ragged lengths and
+a scale other than one.
 """
 import numpy as np
 import pytest
@@ -42,12 +43,12 @@ def _decode_ws(B, S, n, d, w, seed, scale):
 
 @pytest.mark.parametrize("d,w,n,density,scale", [
     (5, 1 << 22, 3_000_017, 0.2, 1.0),           # every task set: one launch over all rows
-    (5, 1 << 22, 3_000_017, 0.0005, 1.0),        # a quarter of the tasks: rows {0,1,2}, {3,4}
+    (5, 1 << 22, 3_000_017, 0.0005, 1.0),        # a quarter of the tasks: rows {0,1}, {2,3,4}
     (5, 1 << 23, 1_000_003, 0.3, 0.5),           # 168 MB: one row per pass
-    (5, 3 * (1 << 20) + 7, 2_000_000, 0.0005, 1.0),  # rows {0,1,2,3}, {4}
-    (5, 5_000_003, 1_500_001, 0.1, 1.0),         # 100 MB: rows {0,1}, {2,3}, {4}
+    (5, 3 * (1 << 20) + 7, 2_000_000, 0.0005, 1.0),  # rows {0}, {1,2,3,4}
+    (5, 5_000_003, 1_500_001, 0.1, 1.0),         # 100 MB: rows {0}, {1,2}, {3,4}
     (3, 5_000_001, 1_048_579, 0.5, 2.0),         # one launch
-    (3, 5_000_001, 1_048_579, 0.001, 2.0),       # rows {0,1}, {2}
+    (3, 5_000_001, 1_048_579, 0.001, 2.0),       # rows {0}, {1,2}
     (3, 1 << 23, 777_777, 1.0, 1.0),             # every position set; 100 MB: one row per pass
 ])
 def test_row_pass_decode_is_bit_exact(d, w, n, density, scale):
