@@ -20,13 +20,18 @@ namespace s2 {
 namespace {
 
 // Insert value `val` of position `i` into every row of the sketch. The
-// reductions carry an evict-last L2 policy: the sketch being built must stay
-// in L2 while the gradient streams past it. SL: only buckets whose flattened
+// reductions carry no L2 policy of their own: the zero fill before the
+// encode stored the sketch's lines evict-last and the gradient streams past
+// with evict-first loads. Measured on GB300 (ms per step, large LM /
+// embedding / top-k): reductions with an evict-last policy on every line
+// 1.613 / 0.514 / 0.242, on a quarter of the lines 1.585 / 0.512 / 0.236,
+// without a policy 1.571 / 0.509 / 0.235; plain zero-fill stores instead
+// cost 18 % on the large LM (1.852). SL: only buckets whose flattened
 // index j*w + b lies in the launch's slice [a.x_lo, a.x_lo + a.x_span) are
 // updated (a sketch larger than L2 is built one slice per pass).
 template <int D, bool SL>
 __device__ __forceinline__ void insert(float* __restrict__ sk, uint32_t i, float val, const EncodeArgs& a,
-                                       const uint32_t* s_kh, const uint32_t* s_ks, uint64_t keep) {
+                                       const uint32_t* s_kh, const uint32_t* s_ks) {
     const int rows = D > 0 ? D : a.d;
 #pragma unroll
     for (int j = 0; j < (D > 0 ? D : kMaxRows); ++j) {
@@ -34,7 +39,7 @@ __device__ __forceinline__ void insert(float* __restrict__ sk, uint32_t i, float
             const uint64_t x = (uint64_t)j * a.w + bucket_of(i, s_kh[j], a.w);
             if (!SL || x - a.x_lo < a.x_span) {
                 const uint32_t sb = signbit_of(i, s_ks[j]);
-                red_add_f32_hint(sk + x, apply_sign(val, sb), keep);
+                red_add_f32(sk + x, apply_sign(val, sb));
             }
         }
     }
@@ -68,8 +73,8 @@ constexpr uint32_t kDenseTask = 32;  // a task with at least this many nonzeros 
 template <int D, bool SL>
 __device__ __forceinline__ void insert_listed(const uint32_t* lpos, const float* lval, uint32_t cnt, int lane,
                                               float* sk, const EncodeArgs& a, const uint32_t* s_kh,
-                                              const uint32_t* s_ks, uint64_t keep) {
-    if ((uint32_t)lane < cnt) insert<D, SL>(sk, lpos[lane], lval[lane], a, s_kh, s_ks, keep);
+                                              const uint32_t* s_ks) {
+    if ((uint32_t)lane < cnt) insert<D, SL>(sk, lpos[lane], lval[lane], a, s_kh, s_ks);
 }
 
 // fp32 rows, 16-byte aligned. Dense tasks (>= kDenseTask nonzeros, e.g. the
@@ -88,7 +93,6 @@ __global__ void __launch_bounds__(kThreads) encode_f32_vec(EncodeArgs a) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t* lpos = s_lpos[warp];
     float* lval = s_lval[warp];
-    const uint64_t keep = policy_evict_last();
     const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
     uint32_t k = 0;
     uint32_t local = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -137,11 +141,11 @@ __global__ void __launch_bounds__(kThreads) encode_f32_vec(EncodeArgs a) {
                 const int slot = __ffs(mask) - 1;
                 mask &= mask - 1;
                 const uint32_t i = (uint32_t)(e0 + (slot >> 2) * 128 + lane * 4 + (slot & 3));
-                insert<D, SL>(sk, i, __uint_as_float(pick16(v, slot)), a, s_kh, s_ks, keep);
+                insert<D, SL>(sk, i, __uint_as_float(pick16(v, slot)), a, s_kh, s_ks);
             }
         } else if (total > 0) {
             if (k != lk && lcount > 0) {  // the list belongs to another worker: drain it first
-                insert_listed<D, SL>(lpos, lval, lcount, lane, a.sketches + (uint64_t)lk * a.dw, a, s_kh, s_ks, keep);
+                insert_listed<D, SL>(lpos, lval, lcount, lane, a.sketches + (uint64_t)lk * a.dw, a, s_kh, s_ks);
                 __syncwarp();
                 lcount = 0;
             }
@@ -155,7 +159,7 @@ __global__ void __launch_bounds__(kThreads) encode_f32_vec(EncodeArgs a) {
             lcount += total;  // at most 31 + 31 < kListCap
             __syncwarp();
             if (lcount >= 32) {
-                insert_listed<D, SL>(lpos, lval, 32, lane, a.sketches + (uint64_t)lk * a.dw, a, s_kh, s_ks, keep);
+                insert_listed<D, SL>(lpos, lval, 32, lane, a.sketches + (uint64_t)lk * a.dw, a, s_kh, s_ks);
                 const uint32_t rest = lcount - 32;
                 uint32_t p = 0;
                 float q = 0.f;
@@ -178,7 +182,7 @@ __global__ void __launch_bounds__(kThreads) encode_f32_vec(EncodeArgs a) {
         for (int u = 0; u < 4; ++u) v[u] = nv[u];
     }
     if (lcount > 0)
-        insert_listed<D, SL>(lpos, lval, lcount, lane, a.sketches + (uint64_t)lk * a.dw, a, s_kh, s_ks, keep);
+        insert_listed<D, SL>(lpos, lval, lcount, lane, a.sketches + (uint64_t)lk * a.dw, a, s_kh, s_ks);
 }
 
 // ---- bf16, 16-byte vector loads --------------------------------------------
@@ -190,7 +194,6 @@ __global__ void __launch_bounds__(kThreads) encode_bf16_vec(EncodeArgs a) {
     __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
     load_keys(a.keys, s_kh, s_ks);
     const int lane = threadIdx.x & 31;
-    const uint64_t keep = policy_evict_last();
     const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
     uint32_t k = 0;
     uint32_t local = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -246,7 +249,7 @@ __global__ void __launch_bounds__(kThreads) encode_bf16_vec(EncodeArgs a) {
             const uint32_t word = (c >> 1) == 0 ? q.x : ((c >> 1) == 1 ? q.y : ((c >> 1) == 2 ? q.z : q.w));
             const uint32_t bits = (c & 1) ? (word & 0xffff0000u) : (word << 16);
             const uint32_t i = (uint32_t)(e0 + (slot >> 3) * 256 + lane * 8 + c);
-            insert<D, SL>(sk, i, __uint_as_float(bits), a, s_kh, s_ks, keep);
+            insert<D, SL>(sk, i, __uint_as_float(bits), a, s_kh, s_ks);
         }
         local += nwarps;
         while (local >= a.tasks_per_worker && k < a.workers) {
@@ -264,7 +267,6 @@ __global__ void __launch_bounds__(kThreads) encode_scalar(EncodeArgs a) {
     __shared__ uint32_t s_kh[kMaxRows], s_ks[kMaxRows];
     load_keys(a.keys, s_kh, s_ks);
     const int lane = threadIdx.x & 31;
-    const uint64_t keep = policy_evict_last();
     const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
     uint32_t k = 0;
     uint32_t local = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -309,7 +311,7 @@ __global__ void __launch_bounds__(kThreads) encode_scalar(EncodeArgs a) {
 #pragma unroll
             for (int s = 1; s < 16; ++s) bits = (slot == s) ? x[s] : bits;
             const uint32_t i = (uint32_t)(e0 + slot * 32 + lane);
-            insert<D, SL>(sk, i, __uint_as_float(bits), a, s_kh, s_ks, keep);
+            insert<D, SL>(sk, i, __uint_as_float(bits), a, s_kh, s_ks);
         }
         local += nwarps;
         while (local >= a.tasks_per_worker && k < a.workers) {

@@ -15,6 +15,10 @@
 // real distributed run would transmit are never formed, which is why this is
 // a separate entry point and not the simulated data-parallel path.
 //
+// The reductions carry no L2 policy: the zero fill stored the sketch's lines
+// evict-last (large LM, 84 MB sketch: 1.323 ms per step with evict-last
+// reductions, 1.277 without; embedding and top-k within 0.5 %).
+//
 // Two layouts: fp32 rows that are 16-byte aligned go through 16-byte vector
 // loads; every other case (bf16, unaligned rows) has lane l load position
 // u*32 + l of the task (u = 0..15) with plain 4- or 2-byte loads.
@@ -32,7 +36,6 @@ __global__ void __launch_bounds__(kThreads) fused_encode_reduce(FusedArgs a) {
     }
     __syncthreads();
     const int lane = threadIdx.x & 31;
-    const uint64_t keep = policy_evict_last();
     const uint64_t ntasks = (a.n + kTaskElems - 1) / kTaskElems;
     const uint64_t nwarps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
     for (uint64_t t = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < ntasks; t += nwarps) {
@@ -84,7 +87,7 @@ __global__ void __launch_bounds__(kThreads) fused_encode_reduce(FusedArgs a) {
             for (int j = 0; j < (D > 0 ? D : kMaxRows); ++j) {
                 if (D > 0 || j < rows) {
                     const uint32_t b = bucket_of(i, s_kh[j], a.w);
-                    red_add_f32_hint(a.sketch + (uint64_t)j * a.w + b, apply_sign(v, signbit_of(i, s_ks[j])), keep);
+                    red_add_f32(a.sketch + (uint64_t)j * a.w + b, apply_sign(v, signbit_of(i, s_ks[j])));
                 }
             }
         }
@@ -120,7 +123,6 @@ __global__ void __launch_bounds__(kThreads) fused_f32_vec(FusedArgs a) {
     }
     __syncthreads();
     const int lane = threadIdx.x & 31;
-    const uint64_t keep = policy_evict_last();
     const uint64_t ntasks = (a.n + kTaskElems - 1) / kTaskElems;
     const uint64_t nwarps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
     const float* grad = static_cast<const float*>(a.grad);
@@ -175,7 +177,7 @@ __global__ void __launch_bounds__(kThreads) fused_f32_vec(FusedArgs a) {
             for (int j = 0; j < (D > 0 ? D : kMaxRows); ++j) {
                 if (D > 0 || j < rows) {
                     const uint32_t b = bucket_of(i, s_kh[j], a.w);
-                    red_add_f32_hint(a.sketch + (uint64_t)j * a.w + b, apply_sign(val, signbit_of(i, s_ks[j])), keep);
+                    red_add_f32(a.sketch + (uint64_t)j * a.w + b, apply_sign(val, signbit_of(i, s_ks[j])));
                 }
             }
         }
