@@ -263,7 +263,7 @@ S2_API s2_status s2_decode_dense_blocks(const uint32_t *block_bitmap, const floa
  *   too small).
  * When the sketch (4*d*w bytes) is larger than 2/5 of this device's L2 cache
  * and d is 3 or 5, the median is taken in passes over groups of whole rows
- * that fit in 2/5 of L2: a first launch writes the zeros of every
+ * that fit in 2/5 of L2, the smallest group first: a first launch writes the zeros of every
  * 512-position stretch without a set bit and lists the others; each pass then
  * reads only its rows for every set position of the listed stretches and
  * carries the candidates for the median that remain (at most 2 for d = 3, 3
